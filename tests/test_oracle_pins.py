@@ -1,0 +1,317 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: hand-worked
+values from the formulas (tests/golden), brute force with exact fractions or
+plain integer loops, closed forms, library routines that the oracle does not
+use, and invariants the pages state. Every oracle function has at least one
+pin that a plausible slip (dropped eps, wrong rounding mode, swapped operand,
+wrong bit order, wrong sign) would fail.
+"""
+import math
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests.golden import as_array, load
+from ternary_weight_linear_06_b300 import workloads as WL
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ----------------------------------------------------------------- rounding
+def test_round_rational_matches_numpy_double_to_float():
+    # numpy's float64 -> float32 conversion is IEEE round-to-nearest-even; for
+    # a double d the exact rational is d itself.
+    rng = random.Random(1)
+    for _ in range(3000):
+        d = rng.uniform(-1, 1) * 2.0 ** rng.randint(-160, 120)
+        d = abs(d)
+        fr = Fraction(d)
+        got = O.round_rational_to_f32(fr.numerator, fr.denominator)
+        want = np.float32(d)
+        assert got.view(np.uint32) == want.view(np.uint32), d
+
+
+def test_round_rational_ties_and_subnormals():
+    two = Fraction(2)
+    cases = [
+        (Fraction(2 ** 24 + 1), 2.0 ** 24),             # tie -> even (down)
+        (Fraction(2 ** 24 + 3), 2.0 ** 24 + 4),         # tie -> even (up)
+        (Fraction(3, 2) * two ** -149, 2.0 ** -148),    # subnormal tie -> even
+        (Fraction(1, 2) * two ** -149, 0.0),            # below half the min -> 0
+        (Fraction(5, 8) * two ** -149, 2.0 ** -149),
+        (Fraction(1, 3), float(np.float32(1.0) / np.float32(3.0))),
+    ]
+    for x, want in cases:
+        got = O.round_rational_to_f32(x.numerator, x.denominator)
+        assert float(got) == want, (x, got, want)
+
+
+# ------------------------------------------------------------------- gamma
+def _gamma_bruteforce(W):
+    a = np.abs(np.asarray(W, np.float32)).ravel()
+    s = sum(Fraction(float(v)) for v in a)
+    r = s / a.size
+    return O.round_rational_to_f32(r.numerator, r.denominator)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_gamma_equals_exact_fraction_bruteforce(seed):
+    rng = np.random.default_rng(seed)
+    # mixed magnitudes incl. subnormals and large values, both signs
+    W = (rng.standard_normal(300) * 10.0 ** rng.uniform(-44, 30, 300)).astype(np.float32)
+    W[:5] = np.array([1e-45, -3e-45, 0.0, -0.0, 1e30], np.float32)
+    assert O.absmean_gamma(W).view(np.uint32) == _gamma_bruteforce(W).view(np.uint32)
+
+
+def test_gamma_config1_bruteforce():
+    W, _ = WL.tiny_case(0)
+    assert O.absmean_gamma(W).view(np.uint32) == _gamma_bruteforce(W).view(np.uint32)
+
+
+def test_gamma_hand_values_and_ties():
+    g = load("hand_rounding.txt")
+    assert O.absmean_gamma(np.array([1, 2, 3, 4], np.float32)) == np.float32(2.5)
+    assert O.absmean_gamma(np.array([-1, 2, -3, 4], np.float32)) == np.float32(2.5)
+    for key in ("a", "b"):
+        W = as_array(g[f"gamma_tie_{key}_w"], np.float64).astype(np.float32)
+        want = as_array(g[f"gamma_tie_{key}"], np.float64).astype(np.float32)[0]
+        assert O.absmean_gamma(W) == want
+
+
+def test_gamma_is_order_independent_where_naive_fp32_is_not():
+    W = np.array([2.0 ** 24] + [1.0] * 64, np.float32)
+    g1 = O.absmean_gamma(W)
+    g2 = O.absmean_gamma(W[::-1].copy())
+    assert g1.view(np.uint32) == g2.view(np.uint32)
+    exact = Fraction(2 ** 24 + 64, 65)
+    assert g1 == O.round_rational_to_f32(exact.numerator, exact.denominator)
+    naive = np.float32(0)
+    for v in W:
+        naive = np.float32(naive + v)
+    assert np.float32(naive / np.float32(65)) != g1   # 2^24 + 1.0 loses each 1.0
+
+
+def test_gamma_closed_form_gaussian():
+    # E|W| = sigma * sqrt(2/pi) for W ~ N(0, sigma^2); SE = sigma*sqrt(1-2/pi)/sqrt(n)
+    sigma, n = 0.02, 1 << 20
+    W = WL.gaussian_weights(1024, 1024, sigma, seed=11)
+    want = sigma * math.sqrt(2 / math.pi)
+    se = sigma * math.sqrt(1 - 2 / math.pi) / math.sqrt(n)
+    assert abs(float(O.absmean_gamma(W)) - want) < 5 * se
+
+
+def test_weight_scale_adds_eps_in_fp32():
+    assert O.weight_scale(np.float32(0.0)) == np.float32(1e-5)
+    g = np.float32(0.10875)
+    assert O.weight_scale(g) == np.float32(g + np.float32(1e-5))
+    assert O.weight_scale(g) != g                       # eps not dropped
+    _, s_w, t = O.pack_weights(np.zeros((4, 8), np.float32))
+    assert s_w == np.float32(1e-5) and not t.any()      # all-zero W stays zero
+
+
+# --------------------------------------------------------------- ternarize
+def test_hand_example_weights():
+    g = load("hand_bitlinear.txt")
+    W = as_array(g["W"], np.float64).astype(np.float32)
+    gamma = O.absmean_gamma(W)
+    assert abs(float(gamma) - 0.10875) < 2e-7 * 0.10875
+    packed, s_w, t = O.pack_weights(W)
+    assert abs(float(s_w) - 0.10876) < 2e-7
+    np.testing.assert_array_equal(t, as_array(g["t"], np.int8))
+    np.testing.assert_array_equal(packed.ravel(), as_array(g["packed"], np.uint8).ravel())
+
+
+def test_roundclip_ties_hand():
+    g = load("hand_rounding.txt")
+    W = as_array(g["ternary_w"], np.float64).astype(np.float32)[None, :]
+    np.testing.assert_array_equal(O.ternarize(W, np.float32(1.0))[0],
+                                  as_array(g["ternary_t"], np.int8))
+
+
+def test_ternary_invariants():
+    W = WL.gaussian_weights(512, 512, 0.02, seed=3, outlier_frac=0.001)
+    _, s_w, t = O.pack_weights(W)
+    assert set(np.unique(t)) <= {-1, 0, 1}
+    # sign symmetry: t(-W) = -t(W) (gamma is unchanged by the sign)
+    _, s_w2, t2 = O.pack_weights(-W)
+    assert s_w2 == s_w
+    np.testing.assert_array_equal(t2, -t)
+    # a constant matrix maps to all ones: W/s_w = c/(c+eps) in (0.5, 1]
+    _, _, tc = O.pack_weights(np.full((3, 8), 0.37, np.float32))
+    assert (tc == 1).all()
+    # positive entries never map to -1 and vice versa
+    assert not ((W > 0) & (t < 0)).any() and not ((W < 0) & (t > 0)).any()
+
+
+def test_zero_fraction_closed_form():
+    # t = 0 iff |W| <= s_w/2 ~ sigma*sqrt(2/pi)/2, so P(t=0) = 2*Phi(sqrt(2/pi)/2) - 1
+    W = WL.gaussian_weights(1024, 1024, 0.02, seed=5)
+    _, _, t = O.pack_weights(W)
+    p = math.erf(math.sqrt(2 / math.pi) / 2 / math.sqrt(2))
+    assert abs(float((t == 0).mean()) - p) < 0.003
+    assert abs(p - 0.3101) < 1e-3
+
+
+def test_pack_codes_hand_and_roundtrip():
+    g = load("hand_rounding.txt")
+    t = as_array(g["pack_t"], np.int8)
+    np.testing.assert_array_equal(O.pack_codes(t).ravel(), as_array(g["pack_bytes"], np.uint8))
+    rng = np.random.default_rng(9)
+    t = rng.integers(-1, 2, size=(7, 64)).astype(np.int8)
+    np.testing.assert_array_equal(O.unpack_codes(O.pack_codes(t), 64), t)
+    # bit order: column k=4b+j sits in bits [2j, 2j+1] of byte b
+    t = np.zeros((1, 8), np.int8) - 1
+    t[0, 5] = 1                       # byte 1, slot 1 -> code 2 << 2
+    assert O.pack_codes(t)[0, 1] == (2 << 2) and O.pack_codes(t)[0, 0] == 0
+
+
+# -------------------------------------------------------------- act quant
+def test_act_quant_hand_and_ties():
+    g = load("hand_bitlinear.txt")
+    q, m = O.quant_act(as_array(g["X"], np.float64).astype(np.float32)[None, :])
+    np.testing.assert_array_equal(q[0], as_array(g["q"], np.int8))
+    assert m[0] == np.float32(2.0)
+    r = load("hand_rounding.txt")
+    q, m = O.quant_act(as_array(r["act_x"], np.float64).astype(np.float32)[None, :])
+    np.testing.assert_array_equal(q[0], as_array(r["act_q"], np.int8))
+
+
+def test_act_quant_invariants():
+    _, X = WL.tiny_case(0)
+    q, m = O.quant_act(X)
+    # the absmax element maps to +-127
+    for i in (0, 1, 3):
+        j = int(np.argmax(np.abs(X[i])))
+        assert abs(int(q[i, j])) == 127 and np.sign(q[i, j]) == np.sign(X[i, j])
+    # an all-zero token stays zero with m = eps
+    assert not q[2].any() and m[2] == np.float32(1e-5)
+    # the 50x outlier row: outlier -> +-127, most others small
+    j = int(np.argmax(np.abs(X[3])))
+    assert abs(X[3, j]) == 50.0 and abs(int(q[3, j])) == 127
+    others = np.delete(q[3], j)
+    assert np.mean(np.abs(others) <= 3) > 0.7
+    # odd symmetry and power-of-two scale invariance (m scales, q does not)
+    q2, m2 = O.quant_act(-X)
+    np.testing.assert_array_equal(q2, -q)
+    q3, m3 = O.quant_act(X[[0, 1, 3]] * np.float32(8.0))
+    np.testing.assert_array_equal(q3, q[[0, 1, 3]])
+    np.testing.assert_array_equal(m3, m[[0, 1, 3]] * np.float32(8.0))
+    # range
+    assert q.min() >= -128 and q.max() <= 127
+
+
+def test_act_quant_matches_torch_formula_reading():
+    # torch (a different library) evaluating the same fp32 expression
+    X = WL.student_t(16, 512, seed=4)
+    q, m = O.quant_act(X)
+    xt = torch.from_numpy(X)
+    mt = torch.clamp(xt.abs().amax(dim=1), min=1e-5)
+    qt = torch.clamp(torch.round((xt * 127.0) / mt[:, None]), -128, 127).to(torch.int8)
+    np.testing.assert_array_equal(q, qt.numpy())
+    np.testing.assert_array_equal(m, mt.numpy())
+
+
+def test_bf16_widening():
+    u = np.array([0x3F80, 0xC000, 0x0001, 0x7F7F, 0x0000, 0x8000], np.uint16)
+    f = O.bf16_bits_to_f32(u)
+    assert f[0] == 1.0 and f[1] == -2.0 and f[2] == np.float32(2.0 ** -133)
+    assert f[4] == 0.0 and np.signbit(f[5])
+    t = torch.from_numpy(u.view(np.int16)).view(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(f.view(np.uint32), t.view(np.uint32))
+
+
+# ------------------------------------------------------------- int matmul
+def test_int_matmul_bruteforce_loops():
+    rng = np.random.default_rng(2)
+    q = rng.integers(-128, 128, size=(3, 40)).astype(np.int8)
+    t = rng.integers(-1, 2, size=(5, 40)).astype(np.int8)
+    acc = O.int_matmul(q, t)
+    assert acc.shape == (3, 5)
+    for i in range(3):
+        for j in range(5):
+            s = 0
+            for k in range(40):
+                if t[j, k] == 1:
+                    s += int(q[i, k])
+                elif t[j, k] == -1:
+                    s -= int(q[i, k])
+            assert acc[i, j] == s
+
+
+def test_int_matmul_float64_library_and_invariants():
+    rng = np.random.default_rng(3)
+    q = rng.integers(-128, 128, size=(6, 2048)).astype(np.int8)
+    t = rng.integers(-1, 2, size=(9, 2048)).astype(np.int8)
+    acc = O.int_matmul(q, t)
+    ref = torch.from_numpy(q.astype(np.float64)) @ torch.from_numpy(t.astype(np.float64)).T
+    np.testing.assert_array_equal(acc, ref.numpy().astype(np.int32))
+    nnz = (t != 0).sum(axis=1)
+    assert (np.abs(acc) <= 128 * nnz[None, :]).all()
+    perm = rng.permutation(2048)
+    np.testing.assert_array_equal(O.int_matmul(q[:, perm], t[:, perm]), acc)
+    # zero weights contribute nothing
+    t0 = t.copy()
+    t0[:, ::2] = 0
+    np.testing.assert_array_equal(O.int_matmul(q, t0), O.int_matmul(q[:, 1::2], t[:, 1::2]))
+
+
+# ---------------------------------------------------------------- dequant
+def test_dequant_hand_and_fp64():
+    g = load("hand_bitlinear.txt")
+    W = as_array(g["W"], np.float64).astype(np.float32)
+    X = as_array(g["X"], np.float64).astype(np.float32)[None, :]
+    _, s_w, t = O.pack_weights(W)
+    Y, acc, q, m = O.forward(X, t, s_w)
+    np.testing.assert_array_equal(acc[0], as_array(g["acc"], np.int32))
+    want = as_array(g["y"], np.float64)
+    assert np.max(np.abs(Y[0] - want) / np.abs(want)) < 1e-6
+    # exact case: s_w = 2, m = 127 gives c = 2 and y = 2 * acc
+    y = O.dequant(np.array([[3, -5, 1 << 20]]), np.float32(2.0), np.array([127.0], np.float32))
+    np.testing.assert_array_equal(y[0], np.array([6, -10, 2 << 20], np.float32))
+    # fp64 recompute
+    rng = np.random.default_rng(4)
+    acc = rng.integers(-3_000_000, 3_000_000, size=(5, 7))
+    m = (10.0 ** rng.uniform(-3, 2, 5)).astype(np.float32)
+    y = O.dequant(acc, np.float32(0.0161), m)
+    ref = acc * (np.float64(np.float32(0.0161)) * m.astype(np.float64)[:, None] / 127.0)
+    assert np.max(np.abs(y - ref) / np.maximum(np.abs(ref), 1e-30)) < 1e-6
+
+
+def test_forward_zero_token_and_packed_path():
+    W, X = WL.tiny_case(0)
+    packed, s_w, t = O.pack_weights(W)
+    Y, acc, q, m = O.forward(X, t, s_w)
+    assert not Y[2].any() and not acc[2].any()
+    Y2 = O.forward_packed(X, packed, s_w)[0]
+    np.testing.assert_array_equal(Y, Y2)
+
+
+# -------------------------------------------------------------------- FFN
+def test_relu2_and_ffn_composition():
+    y = np.array([[-2.0, -0.0, 0.0, 0.5, 3.0]], np.float32)
+    np.testing.assert_array_equal(O.relu2(y), np.array([[0, 0, 0, 0.25, 9.0]], np.float32))
+    rng = np.random.default_rng(6)
+    Wu = WL.gaussian_weights(64, 32, 0.02, seed=7)
+    Wd = WL.gaussian_weights(32, 64, 0.02, seed=8)
+    X = rng.standard_normal((5, 32)).astype(np.float32)
+    _, su, tu = O.pack_weights(Wu)
+    _, sd, td = O.pack_weights(Wd)
+    Y, h = O.ffn(X, tu, su, td, sd)
+    assert (h >= 0).all() and h.shape == (5, 64)
+    y_up = O.forward(X, tu, su)[0]
+    np.testing.assert_array_equal(h, np.where(y_up > 0, y_up * y_up, 0).astype(np.float32))
+    np.testing.assert_array_equal(Y, O.forward(h, td, sd)[0])
+    # requant of h is non-negative
+    qh, _ = O.quant_act(h)
+    assert qh.min() >= 0
+
+
+def test_tie_count_diagnostic():
+    s = np.float32(1.0)
+    W = np.array([[0.5, np.nextafter(np.float32(0.5), np.float32(1)), 0.3, -0.5]], np.float32)
+    assert O.tie_count(W, s) == 3
