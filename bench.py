@@ -1,0 +1,393 @@
+"""Benchmark of the BitLinear forward on B300.
+
+Default workload (N=1): decode, M = 1 token, over the four BitLinear
+projections of a 2B-class layer (q/o 2560->2560, k/v 2560->640, FFN up
+2560->6912, FFN down 6912->2560) for 30 independent layers. One step = the
+120 BitLinear forwards (per-token int8 quantization, packed ternary GEMV,
+dequant) of one decode token, captured once in a CUDA graph and replayed.
+The packed weights of one step (327 MB) exceed the 126 MB L2, so no flush is
+needed between steps. Metric: GB/s of packed weights streamed.
+
+Multi-GPU (torchrun): each rank runs an independent replica (weak scaling);
+value = all ranks' bytes / the slowest rank's time.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the oracle is the reference for this build; it is not tuned).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BitLinear decode GB/s of packed weights (% HBM peak); prefill int8 TOPS (% peak)"
+UNIT = "GB/s"
+SHAPE_ORDER = ["qo", "kv", "up", "down"]
+
+
+def rank_info():
+    r = int(os.environ.get("RANK", "0"))
+    w = int(os.environ.get("WORLD_SIZE", "1"))
+    lr = int(os.environ.get("LOCAL_RANK", str(r)))
+    return r, w, lr
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.lines = []
+            import threading
+
+            def reader():
+                for line in self.proc.stdout:
+                    self.lines.append((time.time(), line.strip()))
+            self.th = threading.Thread(target=reader, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.1 <= r[0] <= (self.t1 or r[0]) + 0.1]
+        use = inside if inside else rows[-3:]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in use if num(p[1]) is not None]
+        smax = [num(p[2]) for _, p in use if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in use for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# --------------------------------------------------------- decode workload
+def build_decode(torch, BL, WL, layers: int, device):
+    """Packs the 30x4 weight matrices and draws the 120 activation rows."""
+    mats = []
+    for layer in range(layers):
+        for shape in SHAPE_ORDER:
+            K, N = WL.SHAPES_2B[shape]
+            W = torch.from_numpy(WL.decode_weights(shape, layer)).to(device)
+            packed, s_w = BL.pack(W)
+            del W
+            X = torch.from_numpy(WL.decode_activations(shape, layer)).to(device)
+            Y = torch.empty((1, N), dtype=torch.float32, device=device)
+            mats.append({"shape": shape, "layer": layer, "K": K, "N": N, "packed": packed, "s_w": s_w, "X": X,
+                         "Y": Y})
+    torch.cuda.synchronize()
+    return mats
+
+
+def packed_bytes(mats):
+    return sum(m["N"] * m["K"] // 4 for m in mats)
+
+
+def gemv_algorithmic_bytes(mats, M=1):
+    # packed weights + int8 activations + fp32 outputs + the per-token scale
+    return sum(m["N"] * m["K"] // 4 + M * m["K"] + 4 * M * m["N"] + 4 * M for m in mats)
+
+
+def time_graph(torch, g, steps, warmup, stream):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import ternary_weight_linear_06_b300 as BL
+    from ternary_weight_linear_06_b300 import workloads as WL
+
+    rank, world, local_rank = rank_info()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    peaks, peak_src = measured_peaks()
+
+    mats = build_decode(torch, BL, WL, args.layers, device)
+    ws = BL.Workspace(max(BL.workspace_bytes(BL.BL_OP_FORWARD, 1, m["N"], m["K"]) for m in mats), device)
+    stream = torch.cuda.Stream(device)
+    bytes_step = packed_bytes(mats)
+
+    # ---- the step: 120 forwards (quant + GEMV each), one CUDA graph
+    def step():
+        for m in mats:
+            BL.forward(m["X"], m["packed"], m["s_w"], out=m["Y"], workspace=ws)
+
+    with torch.cuda.stream(stream):
+        step()                                   # first calls (attribute setup) outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- dominant kernel alone: the 120 GEMVs from pre-quantized activations
+    qs = []
+    for m in mats:
+        q, mm = BL.quant_act(m["X"])
+        qs.append((q, mm))
+    torch.cuda.synchronize()
+
+    def gemv_only():
+        for m, (q, mm) in zip(mats, qs):
+            BL.forward_q8(q, mm, m["packed"], m["s_w"], out=m["Y"], workspace=ws)
+
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        gemv_only()
+    torch.cuda.synchronize()
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[local_rank]
+                    if os.environ.get("CUDA_VISIBLE_DEVICES") else local_rank)
+    clocks = ClockSampler(gpu_index)
+    time.sleep(0.3)
+
+    # warmup
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    if world > 1:
+        dist.barrier()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    t = torch.tensor([elapsed], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed_max = float(t.item())
+    clk = clocks.stop()
+
+    # dominant kernel timing (GEMV only), same stream, CUDA events
+    with torch.cuda.stream(stream):
+        gemv_s = time_graph(torch, g2, max(args.steps, 50), 3, stream)
+    gemv_launches = len(mats) * max(args.steps, 50)
+    gemv_avg_s = gemv_s / gemv_launches
+    alg_bytes_launch = gemv_algorithmic_bytes(mats) / len(mats)
+    achieved = alg_bytes_launch / gemv_avg_s / 1e9
+
+    # end-to-end: pinned host X -> device, graph, device Y -> pinned host
+    xs_host = [torch.empty_like(m["X"], device="cpu").pin_memory() for m in mats]
+    for h, m in zip(xs_host, mats):
+        h.copy_(m["X"].cpu())
+    ys_host = [torch.empty_like(m["Y"], device="cpu").pin_memory() for m in mats]
+    h2d = sum(x.numel() * 4 for x in xs_host)
+    d2h = sum(y.numel() * 4 for y in ys_host)
+    e_steps = max(1, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for h, m in zip(xs_host, mats):
+                m["X"].copy_(h, non_blocking=True)
+            g.replay()
+            for h, m in zip(ys_host, mats):
+                h.copy_(m["Y"], non_blocking=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            for h, m in zip(xs_host, mats):
+                m["X"].copy_(h, non_blocking=True)
+            g.replay()
+            for h, m in zip(ys_host, mats):
+                h.copy_(m["Y"], non_blocking=True)
+        stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+    e2e_value = bytes_step * e_steps / e2e_s / 1e9 * world
+
+    assert BL.workspace_status(ws) == 0, "device-side status word set"
+
+    value = bytes_step * args.steps * world / elapsed_max / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": f"decode M=1, 2B-class projections (q/o 2560x2560, k/v 2560x640, up 2560x6912, "
+                               f"down 6912x2560) x {args.layers} layers", "M": 1, "layers": args.layers,
+                   "forwards_per_step": len(mats), "packed_bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2 (packed weights per step exceed 126 MB)",
+                   "launch": "CUDA graph of the public forward calls, programmatic dependent launch",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (M=1)", "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "alg_bytes_per_launch": round(alg_bytes_launch), "avg_launch_us": round(gemv_avg_s * 1e6, 3)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "pinned host X -> device, graph replay, device Y -> pinned host, every step"},
+        "gpu_launches": 2 * len(mats) * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(mats, args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_decode_sample(mats_host, seconds):
+    """Times oracle forwards over the packed matrices (round robin) for about
+    `seconds`; returns (packed bytes processed, elapsed s, forwards, shapes)."""
+    import oracle as O
+    done = 0
+    nbytes = 0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        m = mats_host[i % len(mats_host)]
+        O.forward_packed(m["X"], m["packed"], m["s_w"])
+        nbytes += m["N"] * m["K"] // 4
+        done += 1
+        i += 1
+        if time.perf_counter() - t0 >= seconds and done >= 4:
+            break
+    return nbytes, time.perf_counter() - t0, done
+
+
+def host_mats_from_device(mats, limit=8):
+    out = []
+    for m in mats[:limit]:
+        out.append({"K": m["K"], "N": m["N"], "packed": m["packed"].cpu().numpy(),
+                    "s_w": np.float32(m["s_w"].cpu().numpy()[0]), "X": m["X"].cpu().numpy()})
+    return out
+
+
+def cpu_baseline(mats, seconds):
+    hm = host_mats_from_device(mats, limit=4)
+    nbytes, el, n = oracle_decode_sample(hm, seconds)
+    return {"value": round(nbytes / el / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} oracle forwards (M=1) round-robin over layer 0's four projections, {el:.1f} s"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same metric, unit and config."""
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    from ternary_weight_linear_06_b300 import workloads as WL
+    import oracle as O
+    hm = []
+    for shape in SHAPE_ORDER:
+        K, N = WL.SHAPES_2B[shape]
+        W = WL.decode_weights(shape, 0)
+        packed, s_w, _ = O.pack_weights(W)
+        hm.append({"K": K, "N": N, "packed": packed, "s_w": s_w, "X": WL.decode_activations(shape, 0)})
+    per = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_decode_sample(hm, per)
+    tot_b = tot_s = 0.0
+    tot_n = 0
+    for _ in range(args.steps):
+        b, s, n = oracle_decode_sample(hm, per)
+        tot_b += b
+        tot_s += s
+        tot_n += n
+    value = tot_b / tot_s / 1e9
+    out = {"metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic", "impl": "reference",
+           "config": {"workload": f"decode M=1, 2B-class projections (q/o 2560x2560, k/v 2560x640, up 2560x6912, "
+                                  f"down 6912x2560) x {args.layers} layers", "M": 1, "layers": args.layers},
+           "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": f"each step: {per:.1f} s of oracle forwards over layer 0's four projections "
+                                      f"({tot_n} forwards in total)"},
+           "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

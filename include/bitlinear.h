@@ -1,0 +1,177 @@
+/*
+ * bitlinear.h - C ABI of the BitLinear forward of BitNet b1.58 on B300 (sm_103a).
+ *
+ * What the calls compute (sources are the pages' titles and sections):
+ *   - "BitNet解读" (markgoyens.top), 模型架构 / 权重量化函数, eqs. (1)-(3):
+ *       gamma = (1/nm) sum |W_ij|;  W~ = RoundClip(W / (gamma + eps), -1, 1).
+ *     Same section, 激活量化: activations scaled per token into [-Qb, Qb],
+ *     symmetric, no zero point (Qb = 127 here).
+ *   - "BitNet b1.58 2B4T Technical Report | Summary", 5.1 GPU Inference (and
+ *     the Chinese translation of the report, 5.1 GPU推理): four ternary values
+ *     are packed into one 8-bit value in HBM, loaded, unpacked on chip and
+ *     multiplied with 8-bit activations.
+ *   - "BitNet解读", 革命性的效率提升: the matmul is integer additions and
+ *     subtractions (+1 adds, -1 subtracts, 0 skips).
+ *   - bitnet.cpp intro (gitcode.csdn.net), 1.1: the result is scaled back
+ *     with the scale factors; the report's section 2 (架构): BitLinear replaces
+ *     torch.nn.Linear, no bias terms, the FFN uses squared ReLU.
+ *
+ * Exact definitions used by every call (fp32 is IEEE round-to-nearest-even):
+ *   gamma  = exact mean of |W| rounded once to fp32;  s_w = fp32(gamma + eps)
+ *   t_nk   = clamp(rint(fp32(W_nk / s_w)), -1, 1)            (int, {-1,0,1})
+ *   packed = byte (n, b) holds t+1 of column k = 4b+j in bits [2j, 2j+1]
+ *   m_i    = max(max_k |x_ik|, eps)
+ *   q_ik   = clamp(rint(fp32(fp32(x_ik * 127) / m_i)), -128, 127)
+ *   acc_in = sum_k q_ik * t_nk                                 (exact int32)
+ *   y_in   = fp32(float(acc_in) * fp32(fp32(s_w * m_i) / 127))
+ *   FFN    : h = y_up > 0 ? fp32(y_up * y_up) : 0, requantized as above,
+ *            then the down projection (no gate, no norm in between).
+ *
+ * Conventions for every call:
+ *   - All tensors are row-major, on the current CUDA device, allocated and
+ *     owned by the caller; the library allocates nothing and keeps no state
+ *     besides per-device attributes it queries once.
+ *   - Every device pointer must be 16-byte aligned (BL_ERR_ALIGN otherwise).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). All work is
+ *     enqueued on it asynchronously; a call returns once the work is queued.
+ *     Scales stay on the device, so no call synchronizes the host.
+ *   - Shapes: M >= 0 and N >= 0 (zero is a valid no-op); K > 0, K % 64 == 0,
+ *     K <= 65536, N * K < 2^31 (BL_ERR_SHAPE otherwise). The K bound keeps
+ *     every partial sum of the contraction an integer below 2^24.
+ *   - Arguments are checked on the host before any launch; nothing is
+ *     launched when a check fails. A failed launch returns BL_ERR_CUDA.
+ *   - `workspace` is scratch device memory of at least
+ *     bitlinear_workspace_bytes(op, ...) bytes. Its first 256 bytes hold a
+ *     sticky device status word: zero them once when the workspace is
+ *     allocated; bitlinear_workspace_status() reads and clears it. Calls that
+ *     share one workspace must be ordered on one stream.
+ *   - Non-finite inputs are outside the contract: results are unspecified
+ *     (bitlinear_pack writes s_w = NaN when W holds Inf or NaN).
+ */
+#ifndef BITLINEAR_H
+#define BITLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BL_API __attribute__((visibility("default")))
+#else
+#define BL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BL_OK = 0,
+  BL_ERR_ARG = 1,          /* null pointer, unknown dtype/op, eps not finite and > 0   */
+  BL_ERR_SHAPE = 2,        /* shape outside the supported range (see above)          */
+  BL_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned                       */
+  BL_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed            */
+  BL_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (see workspace_status) */
+  BL_ERR_UNSUPPORTED = 6,  /* current device is not compute capability 10.3          */
+  BL_ERR_WORKSPACE = 7     /* workspace smaller than bitlinear_workspace_bytes()     */
+} bl_status;
+
+typedef enum { BL_DTYPE_F32 = 0, BL_DTYPE_BF16 = 1 } bl_dtype;
+
+typedef enum {
+  BL_OP_PACK = 0,          /* bitlinear_pack(N, K)                          */
+  BL_OP_FORWARD = 1,       /* bitlinear_forward(M, N, K)                    */
+  BL_OP_FFN = 2            /* bitlinear_ffn(M, N = F (hidden), K = D (model)) */
+} bl_op;
+
+/* Version of this ABI (major * 100 + minor). */
+BL_API int bitlinear_version(void);
+
+/* Human-readable name of a bl_status value. Never NULL. */
+BL_API const char* bitlinear_status_str(int status);
+
+/* Bytes of workspace the call `op` needs for these sizes (0 if the sizes are
+ * invalid). For BL_OP_PACK pass M = 0. */
+BL_API size_t bitlinear_workspace_bytes(int op, int M, int N, int K);
+
+/*
+ * Absmean ternary quantization and 2-bit packing of one weight matrix
+ * ("BitNet解读", 权重量化函数, eqs. (1)-(3); packing per the report's 5.1).
+ *   W        [N, K] fp32, device.
+ *   eps      > 0 (1e-5 in the reference configuration).
+ *   packed   [N, K/4] uint8, device, output (the layout documented above).
+ *   s_w      [1] fp32, device, output: fp32(gamma + eps).
+ *   workspace >= bitlinear_workspace_bytes(BL_OP_PACK, 0, N, K) bytes.
+ * gamma is exact (order-independent), so packed and s_w are bit-exact
+ * functions of W.
+ */
+BL_API bl_status bitlinear_pack(const float* W, int N, int K, float eps,
+                         uint8_t* packed, float* s_w,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Per-token absmax int8 quantization ("BitNet解读", 激活量化).
+ *   X        [M, K] fp32 (x_dtype = BL_DTYPE_F32) or bf16 bits (BL_DTYPE_BF16,
+ *            widened exactly to fp32 first), device.
+ *   q        [M, K] int8, device, output.
+ *   m        [M] fp32, device, output: max(max_k |x_ik|, eps).
+ */
+BL_API bl_status bitlinear_quant_act(const void* X, int x_dtype, int M, int K, float eps,
+                              int8_t* q, float* m, void* stream);
+
+/*
+ * BitLinear forward Y = dequant(quant(X) . T^T) (no bias).
+ *   X        [M, K] fp32 or bf16, device.
+ *   packed   [N, K/4] uint8 from bitlinear_pack; s_w [1] fp32, device.
+ *   Y        [M, N] fp32, device, output.
+ *   acc      [M, N] int32, device, output, or NULL: the exact integer
+ *            accumulators (for checking).
+ *   workspace >= bitlinear_workspace_bytes(BL_OP_FORWARD, M, N, K) bytes.
+ */
+BL_API bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K,
+                            const uint8_t* packed, const float* s_w, int N, float eps,
+                            float* Y, int32_t* acc,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * BitLinear forward on an input that is already quantized: q [M, K] int8 and
+ * m [M] fp32 as written by bitlinear_quant_act (e.g. one quantization shared
+ * by the q, k and v projections, which read the same activations; each
+ * BitLinear quantizes its input the same way, so the result is identical to
+ * bitlinear_forward on the unquantized X). Other arguments as above.
+ */
+BL_API bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K,
+                               const uint8_t* packed, const float* s_w, int N,
+                               float* Y, int32_t* acc,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FFN block of the 2B4T architecture (report section 2: squared ReLU):
+ *   Y = BitLinear_down(ReLU^2(BitLinear_up(X))), ungated, each BitLinear
+ *   quantizing its own input per token.
+ *   X        [M, D] fp32 or bf16; up [F, D/4] uint8 + s_up [1]; down [D, F/4]
+ *            uint8 + s_down [1]; Y [M, D] fp32 output. D and F obey the K rules.
+ *   workspace >= bitlinear_workspace_bytes(BL_OP_FFN, M, F, D) bytes.
+ */
+BL_API bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D,
+                        const uint8_t* up, const float* s_up,
+                        const uint8_t* down, const float* s_down, int F, float eps,
+                        float* Y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Decode packed codes back to ternary values (the inverse of the packing of
+ * the report's 5.1): t [N, K] int8 in {-1, 0, 1} (code 3, never written by
+ * bitlinear_pack, decodes to 2).
+ */
+BL_API bl_status bitlinear_unpack(const uint8_t* packed, int N, int K, int8_t* t, void* stream);
+
+/*
+ * Synchronizes `stream`, reads the sticky status word of `workspace`
+ * (BL_OK or BL_ERR_TIMEOUT), and clears it.
+ */
+BL_API bl_status bitlinear_workspace_status(void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H */

@@ -1,0 +1,247 @@
+// C ABI of the BitLinear library: argument checks, workspace layout and the
+// launch sequence of each call. The kernels live in pack.cu, quant.cu,
+// gemv.cu and gemm_tc.cu.
+#include <atomic>
+#include <cmath>
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace bl {
+namespace {
+
+constexpr int kAbiVersion = 100;
+
+// Per-device capability cache: 0 unknown, 1 compute capability 10.3, -1 other.
+std::atomic<int> g_dev_ok[64];
+
+bl_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BL_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return BL_ERR_UNSUPPORTED;
+  int v = g_dev_ok[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return BL_ERR_CUDA;
+    v = (major == 10 && minor == 3) ? 1 : -1;
+    g_dev_ok[dev].store(v, std::memory_order_relaxed);
+  }
+  return v == 1 ? BL_OK : BL_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_k(int K) { return K > 0 && K % 64 == 0 && K <= kMaxK; }
+
+bool valid_nk(int N, int K) { return N >= 0 && valid_k(K) && static_cast<long long>(N) * K < (1ll << 31); }
+
+bool valid_eps(float eps) { return std::isfinite(eps) && eps > 0.0f; }
+
+bool valid_dtype(int d) { return d == BL_DTYPE_F32 || d == BL_DTYPE_BF16; }
+
+bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
+
+// Forward workspace: header | q (M*K fp16 or int8) | m [M] | qsum [M]
+struct FwdLayout {
+  size_t q, m, qsum, total;
+};
+FwdLayout fwd_layout(int M, int K) {
+  FwdLayout L;
+  L.q = sizeof(WsHeader);
+  L.m = align_up(L.q + static_cast<size_t>(M) * K * 2, 256);
+  L.qsum = align_up(L.m + 4 * static_cast<size_t>(M), 256);
+  L.total = align_up(L.qsum + 4 * static_cast<size_t>(M), 256);
+  return L;
+}
+
+// FFN workspace: header | qx | mx | qsx | h [M*F] | hmax [M] | qh | mh | qsh
+struct FfnLayout {
+  size_t qx, mx, qsx, h, hmax, qh, mh, qsh, total;
+};
+FfnLayout ffn_layout(int M, int D, int F) {
+  FfnLayout L;
+  const size_t m4 = 4 * static_cast<size_t>(M);
+  L.qx = sizeof(WsHeader);
+  L.mx = align_up(L.qx + static_cast<size_t>(M) * D * 2, 256);
+  L.qsx = align_up(L.mx + m4, 256);
+  L.h = align_up(L.qsx + m4, 256);
+  L.hmax = align_up(L.h + static_cast<size_t>(M) * F * 4, 256);
+  L.qh = align_up(L.hmax + m4, 256);
+  L.mh = align_up(L.qh + static_cast<size_t>(M) * F * 2, 256);
+  L.qsh = align_up(L.mh + m4, 256);
+  L.total = align_up(L.qsh + m4, 256);
+  return L;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+// One BitLinear on an already-quantized input (int8 row-major q, scales m).
+bl_status run_linear(const int8_t* q, const float* m, int M, int K, const uint8_t* packed, const float* s_w, int N,
+                     float* Y, int32_t* acc, Epi epi, float* absmax_out, cudaStream_t st) {
+  return from_cuda(launch_gemv(packed, N, K, q, m, s_w, M, Y, acc, epi, absmax_out, true, st));
+}
+
+bl_status check_linear_args(int M, int K, const uint8_t* packed, const float* s_w, int N, const float* Y,
+                            const int32_t* acc, void* workspace, size_t workspace_bytes) {
+  if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
+  if (M == 0 || N == 0) return BL_OK;
+  if (!packed || !s_w || !Y || !workspace) return BL_ERR_ARG;
+  if (!aligned16(packed) || !aligned16(Y) || !aligned16(workspace) || (acc && !aligned16(acc)) ||
+      (reinterpret_cast<uintptr_t>(s_w) & 3u))
+    return BL_ERR_ALIGN;
+  if (workspace_bytes < bitlinear_workspace_bytes(BL_OP_FORWARD, M, N, K)) return BL_ERR_WORKSPACE;
+  return check_device();
+}
+
+}  // namespace
+}  // namespace bl
+
+using namespace bl;
+
+extern "C" {
+
+int bitlinear_version(void) { return kAbiVersion; }
+
+const char* bitlinear_status_str(int status) {
+  switch (status) {
+    case BL_OK: return "BL_OK";
+    case BL_ERR_ARG: return "BL_ERR_ARG: invalid argument";
+    case BL_ERR_SHAPE: return "BL_ERR_SHAPE: unsupported shape";
+    case BL_ERR_ALIGN: return "BL_ERR_ALIGN: pointer not 16-byte aligned";
+    case BL_ERR_CUDA: return "BL_ERR_CUDA: CUDA call or launch failed";
+    case BL_ERR_TIMEOUT: return "BL_ERR_TIMEOUT: device-side wait gave up";
+    case BL_ERR_UNSUPPORTED: return "BL_ERR_UNSUPPORTED: device is not compute capability 10.3";
+    case BL_ERR_WORKSPACE: return "BL_ERR_WORKSPACE: workspace too small";
+    default: return "unknown bl_status";
+  }
+}
+
+size_t bitlinear_workspace_bytes(int op, int M, int N, int K) {
+  switch (op) {
+    case BL_OP_PACK:
+      if (!valid_nk(N, K) || N == 0) return 0;
+      return sizeof(WsHeader) + pack_scratch_bytes();
+    case BL_OP_FORWARD:
+      if (M < 0 || !valid_nk(N, K)) return 0;
+      return fwd_layout(M, K).total;
+    case BL_OP_FFN:
+      if (M < 0 || !valid_nk(N, K) || !valid_k(N) || N == 0) return 0;
+      return ffn_layout(M, K, N).total;
+    default: return 0;
+  }
+}
+
+bl_status bitlinear_pack(const float* W, int N, int K, float eps, uint8_t* packed, float* s_w, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!W || !packed || !s_w || !workspace) return BL_ERR_ARG;
+  if (!valid_eps(eps)) return BL_ERR_ARG;
+  if (!valid_nk(N, K) || N == 0) return BL_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(packed) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(s_w) & 3u))
+    return BL_ERR_ALIGN;
+  if (workspace_bytes < bitlinear_workspace_bytes(BL_OP_PACK, 0, N, K)) return BL_ERR_WORKSPACE;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  return from_cuda(launch_pack(W, N, K, eps, packed, s_w, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+bl_status bitlinear_quant_act(const void* X, int x_dtype, int M, int K, float eps, int8_t* q, float* m,
+                              void* stream) {
+  if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
+  if (M < 0 || !valid_k(K)) return BL_ERR_SHAPE;
+  if (M == 0) return BL_OK;
+  if (!X || !q || !m) return BL_ERR_ARG;
+  if (!aligned16(X) || !aligned16(q) || !aligned16(m)) return BL_ERR_ALIGN;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, false,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K, const uint8_t* packed, const float* s_w, int N,
+                            float eps, float* Y, int32_t* acc, void* workspace, size_t workspace_bytes,
+                            void* stream) {
+  if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
+  if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
+  if (M == 0 || N == 0) return BL_OK;
+  if (!X) return BL_ERR_ARG;
+  if (!aligned16(X)) return BL_ERR_ALIGN;
+  if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
+    return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FwdLayout L = fwd_layout(M, K);
+  int8_t* q = at<int8_t>(workspace, L.q);
+  float* m = at<float>(workspace, L.m);
+  if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, true, st) != cudaSuccess)
+    return BL_ERR_CUDA;
+  return run_linear(q, m, M, K, packed, s_w, N, Y, acc, Epi::kPlain, nullptr, st);
+}
+
+bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, const uint8_t* packed, const float* s_w,
+                               int N, float* Y, int32_t* acc, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
+  if (M == 0 || N == 0) return BL_OK;
+  if (!q || !m) return BL_ERR_ARG;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(m) & 3u)) return BL_ERR_ALIGN;
+  if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
+    return s;
+  return run_linear(q, m, M, K, packed, s_w, N, Y, acc, Epi::kPlain, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
+                        const uint8_t* down, const float* s_down, int F, float eps, float* Y, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
+  if (M < 0 || !valid_nk(F, D) || !valid_nk(D, F) || F == 0) return BL_ERR_SHAPE;
+  if (M == 0) return BL_OK;
+  if (!X || !up || !s_up || !down || !s_down || !Y || !workspace) return BL_ERR_ARG;
+  if (!aligned16(X) || !aligned16(up) || !aligned16(down) || !aligned16(Y) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(s_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u))
+    return BL_ERR_ALIGN;
+  if (workspace_bytes < bitlinear_workspace_bytes(BL_OP_FFN, M, F, D)) return BL_ERR_WORKSPACE;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FfnLayout L = ffn_layout(M, D, F);
+  int8_t* qx = at<int8_t>(workspace, L.qx);
+  float* mx = at<float>(workspace, L.mx);
+  float* h = at<float>(workspace, L.h);
+  float* hmax = at<float>(workspace, L.hmax);
+  int8_t* qh = at<int8_t>(workspace, L.qh);
+  float* mh = at<float>(workspace, L.mh);
+  cudaError_t e = cudaMemsetAsync(hmax, 0, 4 * static_cast<size_t>(M), st);
+  if (e != cudaSuccess) return BL_ERR_CUDA;
+  e = launch_quant(X, x_dtype, M, D, eps, QLayout::kRowMajorI8, qx, mx, nullptr, nullptr, false, st);
+  if (e != cudaSuccess) return BL_ERR_CUDA;
+  bl_status s = run_linear(qx, mx, M, D, up, s_up, F, h, nullptr, Epi::kRelu2, hmax, st);
+  if (s != BL_OK) return s;
+  e = launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kRowMajorI8, qh, mh, nullptr, hmax, true, st);
+  if (e != cudaSuccess) return BL_ERR_CUDA;
+  return run_linear(qh, mh, M, F, down, s_down, D, Y, nullptr, Epi::kPlain, nullptr, st);
+}
+
+bl_status bitlinear_unpack(const uint8_t* packed, int N, int K, int8_t* t, void* stream) {
+  if (!valid_nk(N, K)) return BL_ERR_SHAPE;
+  if (N == 0) return BL_OK;
+  if (!packed || !t) return BL_ERR_ARG;
+  if (!aligned16(packed) || !aligned16(t)) return BL_ERR_ALIGN;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  return from_cuda(launch_unpack(packed, N, K, t, static_cast<cudaStream_t>(stream)));
+}
+
+bl_status bitlinear_workspace_status(void* workspace, void* stream) {
+  if (!workspace) return BL_ERR_ARG;
+  if (!aligned16(workspace)) return BL_ERR_ALIGN;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader h;
+  if (cudaMemcpyAsync(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return BL_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return BL_ERR_CUDA;
+  if (h.status == 0) return BL_OK;
+  if (cudaMemsetAsync(workspace, 0, sizeof(WsHeader), st) != cudaSuccess) return BL_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return BL_ERR_CUDA;
+  return static_cast<bl_status>(h.status);
+}
+
+}  // extern "C"

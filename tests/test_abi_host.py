@@ -1,0 +1,83 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from ternary_weight_linear_06_b300 import _lib
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "bitlinear.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"BL_API\s+[\w\s\*]+?\b(bitlinear_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared()
+    assert len(names) >= 9
+    lib = _lib.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(_lib.SIGNATURES), "binding misses a declared entry point"
+
+
+def test_version_and_status_strings():
+    lib = _lib.lib()
+    assert lib.bitlinear_version() == 100
+    for s in range(8):
+        assert lib.bitlinear_status_str(s)
+    assert b"unknown" in lib.bitlinear_status_str(99)
+
+
+def test_workspace_bytes_rules():
+    f = _lib.lib().bitlinear_workspace_bytes
+    assert f(_lib.BL_OP_FORWARD, 4, 256, 256) >= 256 + 4 * 256 * 2
+    assert f(_lib.BL_OP_FORWARD, 4, 256, 100) == 0          # K % 64 != 0
+    assert f(_lib.BL_OP_FORWARD, -1, 256, 256) == 0
+    assert f(_lib.BL_OP_FORWARD, 1, 256, 65536 + 64) == 0   # K above the exactness bound
+    assert f(_lib.BL_OP_FORWARD, 1, 1 << 16, 1 << 15) == 0  # N*K >= 2^31
+    assert f(_lib.BL_OP_PACK, 0, 0, 256) == 0
+    assert f(_lib.BL_OP_PACK, 0, 256, 256) > 256
+    assert f(_lib.BL_OP_FFN, 8, 6912, 2560) > 8 * 6912 * 4
+    assert f(99, 1, 1, 64) == 0
+
+
+def test_host_argument_checks_fail_before_launch():
+    lib = _lib.lib()
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16        # a 16-byte aligned host address, never dereferenced
+    # null pointers
+    assert lib.bitlinear_pack(None, 4, 64, 1e-5, p, p, p, 4096, None) == _lib.BL_ERR_ARG
+    # bad eps
+    assert lib.bitlinear_pack(p, 4, 64, 0.0, p, p, p, 4096, None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_pack(p, 4, 64, float("nan"), p, p, p, 4096, None) == _lib.BL_ERR_ARG
+    # shapes
+    assert lib.bitlinear_pack(p, 4, 100, 1e-5, p, p, p, 4096, None) == _lib.BL_ERR_SHAPE
+    assert lib.bitlinear_pack(p, 0, 64, 1e-5, p, p, p, 4096, None) == _lib.BL_ERR_SHAPE
+    assert lib.bitlinear_forward(p, 0, 1, 96, p, p, 4, 1e-5, p, None, p, 4096, None) == _lib.BL_ERR_SHAPE
+    assert lib.bitlinear_forward(p, 0, -1, 64, p, p, 4, 1e-5, p, None, p, 4096, None) == _lib.BL_ERR_SHAPE
+    # bad dtype
+    assert lib.bitlinear_forward(p, 7, 1, 64, p, p, 4, 1e-5, p, None, p, 4096, None) == _lib.BL_ERR_ARG
+    # misaligned pointers
+    assert lib.bitlinear_forward(p + 4, 0, 1, 64, p, p, 4, 1e-5, p, None, p, 4096, None) == _lib.BL_ERR_ALIGN
+    assert lib.bitlinear_pack(p, 4, 64, 1e-5, p + 8, p, p, 4096, None) == _lib.BL_ERR_ALIGN
+    # workspace too small
+    assert lib.bitlinear_forward(p, 0, 1, 64, p, p, 4, 1e-5, p, None, p, 16, None) == _lib.BL_ERR_WORKSPACE
+    assert lib.bitlinear_ffn(p, 0, 2, 64, p, p, p, p, 128, 1e-5, p, p, 16, None) == _lib.BL_ERR_WORKSPACE
+    # empty problems are a no-op that touches nothing
+    assert lib.bitlinear_forward(None, 0, 0, 64, None, None, 4, 1e-5, None, None, None, 0, None) == _lib.BL_OK
+    assert lib.bitlinear_forward(None, 0, 3, 64, None, None, 0, 1e-5, None, None, None, 0, None) == _lib.BL_OK
+    assert lib.bitlinear_quant_act(None, 0, 0, 64, 1e-5, None, None, None) == _lib.BL_OK
+    assert lib.bitlinear_workspace_status(None, None) == _lib.BL_ERR_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib()

@@ -1,0 +1,200 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Bar: packed codes, s_w, int8 activations and int32 accumulators bit-exact;
+fp32 outputs within 1e-5 relative (the contract) -- the kernels perform the
+same fp32 operations in the same order as the oracle, so the tests also
+check that Y is bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import ternary_weight_linear_06_b300 as BL
+from ternary_weight_linear_06_b300 import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def assert_y(Y_gpu, Y_ref):
+    Y_gpu = np.asarray(Y_gpu, np.float32)
+    Y_ref = np.asarray(Y_ref, np.float32)
+    rel = np.abs(Y_gpu.astype(np.float64) - Y_ref) / np.maximum(np.abs(Y_ref.astype(np.float64)), 1e-30)
+    assert rel.max(initial=0.0) <= RTOL, rel.max()
+    np.testing.assert_array_equal(Y_gpu.view(np.uint32), Y_ref.view(np.uint32))
+
+
+# ----------------------------------------------------------------- packing
+def check_pack(W):
+    packed, s_w = BL.pack(dev(W))
+    p_ref, s_ref, t_ref = O.pack_weights(W)
+    assert host(s_w).view(np.uint32)[0] == np.float32(s_ref).view(np.uint32), (host(s_w)[0], s_ref)
+    np.testing.assert_array_equal(host(packed), p_ref)
+    np.testing.assert_array_equal(host(BL.unpack(packed, W.shape[1])), t_ref)
+    return packed, s_w, t_ref, s_ref
+
+
+def test_pack_tiny():
+    W, _ = WL.tiny_case(0)
+    check_pack(W)
+
+
+@pytest.mark.parametrize("shape", ["kv", "qo", "up", "down"])
+def test_pack_decode_shapes(shape):
+    check_pack(WL.decode_weights(shape, 0))
+
+
+def test_pack_exponent_extremes_and_ties():
+    rng = np.random.default_rng(21)
+    W = (rng.standard_normal((64, 256)) * 0.02).astype(np.float32)
+    # values outside the 128-bit window: subnormals, tiny normals, huge values
+    W[0, :8] = np.array([1e-45, -2e-44, 3e-39, -1e-38, 1e-20, 3e15, -7e25, 2e30], np.float32)
+    check_pack(W)
+    # exact ternary ties: entries equal to +-s_w/2 for the matrix's own s_w
+    W = (rng.standard_normal((128, 512)) * 0.02).astype(np.float32)
+    for _ in range(3):
+        s = O.pack_weights(W)[1]
+        W[np.arange(0, 128, 2), 7] = np.float32(s) * np.float32(0.5)
+        W[np.arange(1, 128, 2), 9] = -np.float32(s) * np.float32(0.5)
+        W[5, 11] = np.nextafter(np.float32(s) * np.float32(0.5), np.float32(1))
+    s = O.pack_weights(W)[1]
+    assert O.tie_count(W, s) > 0
+    check_pack(W)
+
+
+def test_pack_nonfinite_gives_nan_scale():
+    W = np.ones((4, 64), np.float32)
+    W[1, 3] = np.inf
+    _, s_w = BL.pack(dev(W))
+    assert np.isnan(host(s_w)[0])
+
+
+# ------------------------------------------------------------ quantization
+def test_quant_act_f32_and_bf16():
+    _, X = WL.tiny_case(0)
+    q, m = BL.quant_act(dev(X))
+    q_ref, m_ref = O.quant_act(X)
+    np.testing.assert_array_equal(host(q), q_ref)
+    np.testing.assert_array_equal(host(m).view(np.uint32), m_ref.view(np.uint32))
+    xb = WL.batched_activations_bf16(16, 2560, seed=31)
+    Xb = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    q, m = BL.quant_act(Xb)
+    q_ref, m_ref = O.quant_act(O.bf16_bits_to_f32(xb))
+    np.testing.assert_array_equal(host(q), q_ref)
+    np.testing.assert_array_equal(host(m), m_ref)
+
+
+# ----------------------------------------------------------------- forward
+def check_forward(W, X, x_is_bf16_bits=False):
+    packed, s_w, t_ref, s_ref = check_pack(W)
+    if x_is_bf16_bits:
+        Xd = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+        Xf = O.bf16_bits_to_f32(X)
+    else:
+        Xd, Xf = dev(X), X
+    Y, acc = BL.forward(Xd, packed, s_w, return_acc=True)
+    Y_ref, acc_ref, _, _ = O.forward(Xf, t_ref, s_ref)
+    np.testing.assert_array_equal(host(acc), acc_ref)
+    assert_y(host(Y), Y_ref)
+
+
+def test_forward_tiny_case():
+    W, X = WL.tiny_case(0)
+    check_forward(W, X)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 16, 17])
+def test_forward_token_counts_ragged_rows(M):
+    # N = 203 rows is ragged for every row-group size; K = 320 spans several 16-byte chunks per lane pass
+    W = WL.gaussian_weights(203, 320, 0.02, seed=40 + M, outlier_frac=0.01)
+    X = WL.student_t(M, 320, seed=60 + M)
+    X[0, :5] = 0.0
+    check_forward(W, X)
+
+
+@pytest.mark.parametrize("K", [64, 128, 2048, 2112, 4096])
+def test_forward_k_sizes(K):
+    W = WL.gaussian_weights(70, K, 0.02, seed=K)
+    X = WL.student_t(3, K, seed=K + 1)
+    check_forward(W, X)
+
+
+def test_forward_bf16_input_batched():
+    W = WL.decode_weights("kv", 3)
+    xb = WL.batched_activations_bf16(4, 2560, seed=77)
+    check_forward(W, xb, x_is_bf16_bits=True)
+
+
+def test_forward_zero_and_extreme_tokens():
+    W = WL.gaussian_weights(96, 256, 0.02, seed=5)
+    X = np.zeros((4, 256), np.float32)
+    X[1] = 1e-30                      # below eps: m = eps, q = 0
+    X[2, 3] = 1e30                    # single huge entry
+    X[3] = WL.student_t(1, 256, seed=6)[0] * np.float32(1e6)
+    check_forward(W, X)
+
+
+def test_forward_empty_is_noop():
+    W = WL.gaussian_weights(32, 64, 0.02, seed=1)
+    packed, s_w = BL.pack(dev(W))
+    Y = BL.forward(torch.zeros((0, 64), device="cuda"), packed, s_w)
+    assert Y.shape == (0, 32)
+
+
+@pytest.mark.parametrize("shape", ["kv", "qo", "up", "down"])
+def test_forward_decode_full_size_m1(shape):
+    W = WL.decode_weights(shape, 1)
+    X = WL.decode_activations(shape, 1)
+    check_forward(W, X)
+
+
+# --------------------------------------------------------------------- FFN
+def test_ffn_small():
+    D, F, M = 256, 512, 6
+    Wu = WL.gaussian_weights(F, D, 0.02, seed=90, outlier_frac=0.001)
+    Wd = WL.gaussian_weights(D, F, 0.02, seed=91, outlier_frac=0.001)
+    X = WL.prefill_activations(M, D, seed=92)
+    up, s_up = BL.pack(dev(Wu))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sd, td = O.pack_weights(Wd)
+    Y = BL.ffn(dev(X), up, s_up, down, s_down)
+    Y_ref, _ = O.ffn(X, tu, su, td, sd)
+    assert_y(host(Y), Y_ref)
+
+
+def test_workspace_status_clean():
+    assert BL.workspace_status() == 0
+
+
+def test_forward_q8_shared_quantization():
+    # q/k/v style: one quantization, three projections
+    X = WL.decode_activations("qo", 2, M=3)
+    q, m = BL.quant_act(dev(X))
+    q_ref, m_ref = O.quant_act(X)
+    np.testing.assert_array_equal(host(q), q_ref)
+    for shape in ("qo", "kv"):
+        W = WL.decode_weights(shape, 2)
+        packed, s_w, t_ref, s_ref = check_pack(W)
+        Y, acc = BL.forward_q8(q, m, packed, s_w, return_acc=True)
+        acc_ref = O.int_matmul(q_ref, t_ref)
+        np.testing.assert_array_equal(host(acc), acc_ref)
+        assert_y(host(Y), O.dequant(acc_ref, s_ref, m_ref))
+        Y2 = BL.forward(dev(X), packed, s_w)
+        np.testing.assert_array_equal(host(Y2), host(Y))
