@@ -145,6 +145,36 @@ BL_API bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, in
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Size of the fixed device scratch array behind bitlinear_forward_noalloc.
+ */
+#define BL_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * bitlinear_forward without a workspace argument. The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory when they run the forward (a runtime that fixes its memory
+ * plan at start-up, a plugin whose host framework owns all device memory).
+ * It computes exactly what bitlinear_forward computes, with the same launch
+ * sequence, and calls no cudaMalloc, cudaFree or other allocating routine.
+ *   Scratch: a library-owned array of BL_STATIC_SCRATCH_BYTES (8 MiB) in device
+ *     global memory, present on every GPU that loads the library until the
+ *     process exits. Sizes whose bitlinear_workspace_bytes(BL_OP_FORWARD, M, N,
+ *     K) exceeds it return BL_ERR_WORKSPACE before any launch (e.g. M * K up to
+ *     about 4 million activations).
+ *   The first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress (set-up); make that first call before any stream
+ *     capture.
+ *   All calls on a device share the one array, and it keeps the last call's
+ *     contents (nothing in it has to start at zero: each call writes its
+ *     scratch before reading it). Calls that overlap on the GPU (e.g. on two
+ *     streams without ordering) race on it: order them.
+ *   Other arguments, checks and error codes as for bitlinear_forward.
+ */
+BL_API bl_status bitlinear_forward_noalloc(const void* X, int x_dtype, int M, int K,
+                                    const uint8_t* packed, const float* s_w, int N, float eps,
+                                    float* Y, int32_t* acc, void* stream);
+
+/*
  * FFN block of the 2B4T architecture (report section 2: squared ReLU):
  *   Y = BitLinear_down(ReLU^2(BitLinear_up(X))), ungated, each BitLinear
  *   quantizing its own input per token.

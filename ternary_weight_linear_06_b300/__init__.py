@@ -19,7 +19,7 @@ from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_OP_FFN, BL_OP_FORWARD, BL_OP_
 
 EPS = 1e-5
 
-__all__ = ["pack", "quant_act", "forward", "forward_q8", "ffn", "unpack", "workspace_bytes", "workspace_status",
+__all__ = ["pack", "quant_act", "forward", "forward_q8", "forward_noalloc", "ffn", "unpack", "workspace_bytes", "workspace_status",
            "Workspace", "BitLinearError", "EPS", "library_path"]
 
 
@@ -141,6 +141,26 @@ def forward_q8(q: torch.Tensor, m: torch.Tensor, packed: torch.Tensor, s_w: torc
     ws = _workspace(workspace, nb)
     check(_lib.lib().bitlinear_forward_q8(_ptr(q), _ptr(m), M, K, _ptr(packed), _ptr(s_w), N, _ptr(Y), _ptr(acc),
                                           _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_forward_q8")
+    return (Y, acc) if return_acc else Y
+
+
+def forward_noalloc(X: torch.Tensor, packed: torch.Tensor, s_w: torch.Tensor, eps: float = EPS,
+                    return_acc: bool = False, out: torch.Tensor | None = None, stream=None):
+    """forward() for callers that cannot provide device scratch: the library
+    uses its own fixed 8 MiB device array instead of a workspace. The first
+    call on a device does a one-time address lookup (make it before any stream
+    capture); calls that overlap on the GPU race on the shared array."""
+    _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+    _need_cuda(packed, "packed", (torch.uint8,))
+    _need_cuda(s_w, "s_w", (torch.float32,))
+    M, K = X.shape
+    N = packed.shape[0]
+    if packed.shape[1] * 4 != K:
+        raise ValueError(f"packed has {packed.shape[1]} bytes per row, expected K/4 = {K // 4}")
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=X.device)
+    acc = torch.empty((M, N), dtype=torch.int32, device=X.device) if return_acc else None
+    check(_lib.lib().bitlinear_forward_noalloc(_ptr(X), _x_dtype(X), M, K, _ptr(packed), _ptr(s_w), N, eps,
+                                               _ptr(Y), _ptr(acc), _stream(stream)), "bitlinear_forward_noalloc")
     return (Y, acc) if return_acc else Y
 
 

@@ -22,6 +22,8 @@ BL_ERR_WORKSPACE = 7
 BL_DTYPE_F32 = 0
 BL_DTYPE_BF16 = 1
 
+BL_STATIC_SCRATCH_BYTES = 8 << 20
+
 BL_OP_PACK = 0
 BL_OP_FORWARD = 1
 BL_OP_FFN = 2
@@ -37,6 +39,7 @@ SIGNATURES = {
     "bitlinear_quant_act": (_i, [_vp, _i, _i, _i, _f, _vp, _vp, _vp]),
     "bitlinear_forward": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp, _sz, _vp]),
     "bitlinear_forward_q8": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+    "bitlinear_forward_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp]),
     "bitlinear_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "bitlinear_unpack": (_i, [_vp, _i, _i, _vp, _vp]),
     "bitlinear_workspace_status": (_i, [_vp, _vp]),
