@@ -80,7 +80,8 @@ typedef enum { BL_DTYPE_F32 = 0, BL_DTYPE_BF16 = 1 } bl_dtype;
 typedef enum {
   BL_OP_PACK = 0,          /* bitlinear_pack(N, K)                          */
   BL_OP_FORWARD = 1,       /* bitlinear_forward(M, N, K)                    */
-  BL_OP_FFN = 2            /* bitlinear_ffn(M, N = F (hidden), K = D (model)) */
+  BL_OP_FFN = 2,           /* bitlinear_ffn(M, N = F (hidden), K = D (model)) */
+  BL_OP_FORWARD_BATCH = 3  /* bitlinear_forward_batch (sizes ignored)       */
 } bl_op;
 
 /* Version of this ABI (major * 100 + minor). */
@@ -131,6 +132,40 @@ BL_API bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K,
                             const uint8_t* packed, const float* s_w, int N, float eps,
                             float* Y, int32_t* acc,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One problem of bitlinear_forward_batch: the arguments of one
+ * bitlinear_forward call (all pointers on the device).
+ */
+typedef struct {
+  const void* X;            /* [M, K] fp32 or bf16                       */
+  int x_dtype;              /* BL_DTYPE_F32 or BL_DTYPE_BF16             */
+  int M;                    /* tokens (>= 0)                             */
+  int K;                    /* input features                            */
+  int N;                    /* output features (>= 0)                    */
+  const uint8_t* packed;    /* [N, K/4] from bitlinear_pack              */
+  const float* s_w;         /* [1]                                       */
+  float* Y;                 /* [M, N] output                             */
+  int32_t* acc;             /* [M, N] int32 output, or NULL              */
+} bl_forward_desc;
+
+#define BL_MAX_BATCH 128
+
+/*
+ * `count` independent BitLinear forwards in one launch sequence (e.g. the
+ * q, k and v projections of a layer, or the projections of several
+ * independent sequences): each result equals that of bitlinear_forward on
+ * the same arguments. No problem may read another's outputs. The packed
+ * weights of all problems stream through one persistent grid, so small
+ * matrices do not each pay a launch and a pipeline ramp.
+ *   descs     host array of `count` descriptors (0 <= count <= BL_MAX_BATCH),
+ *             read during the call only.
+ *   workspace >= bitlinear_workspace_bytes(BL_OP_FORWARD_BATCH, 0, 0, 0) bytes.
+ * Each descriptor is checked like bitlinear_forward's arguments; the first
+ * failing check is returned and nothing is launched.
+ */
+BL_API bl_status bitlinear_forward_batch(const bl_forward_desc* descs, int count, float eps,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * BitLinear forward on an input that is already quantized: q [M, K] int8 and

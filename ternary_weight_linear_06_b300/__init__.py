@@ -14,12 +14,12 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_OP_FFN, BL_OP_FORWARD, BL_OP_PACK, BitLinearError,  # noqa: F401
-                   check)
+from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_MAX_BATCH, BL_OP_FFN, BL_OP_FORWARD,  # noqa: F401
+                   BL_OP_FORWARD_BATCH, BL_OP_PACK, BitLinearError, ForwardDesc, check)
 
 EPS = 1e-5
 
-__all__ = ["pack", "quant_act", "forward", "forward_q8", "forward_noalloc", "ffn", "unpack", "workspace_bytes", "workspace_status",
+__all__ = ["pack", "quant_act", "forward", "forward_batch", "forward_q8", "forward_noalloc", "ffn", "unpack", "workspace_bytes", "workspace_status",
            "Workspace", "BitLinearError", "EPS", "library_path"]
 
 
@@ -122,6 +122,34 @@ def forward(X: torch.Tensor, packed: torch.Tensor, s_w: torch.Tensor, eps: float
     check(_lib.lib().bitlinear_forward(_ptr(X), _x_dtype(X), M, K, _ptr(packed), _ptr(s_w), N, eps, _ptr(Y),
                                        _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_forward")
     return (Y, acc) if return_acc else Y
+
+
+def forward_batch(problems, eps: float = EPS, workspace: Workspace | None = None, stream=None, descs=None):
+    """Independent BitLinear forwards in one call. `problems` is a sequence of
+    (X, packed, s_w, Y) or (X, packed, s_w, Y, acc) with device tensors; the
+    outputs Y (and acc) are written in place. Returns the ctypes descriptor
+    array, which can be passed back as `descs` to skip rebuilding it."""
+    if descs is None:
+        if len(problems) > BL_MAX_BATCH:
+            raise ValueError(f"at most {BL_MAX_BATCH} problems per call")
+        descs = (ForwardDesc * len(problems))()
+        for d, prob in zip(descs, problems):
+            X, packed, s_w, Y = prob[:4]
+            acc = prob[4] if len(prob) > 4 else None
+            _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+            _need_cuda(packed, "packed", (torch.uint8,))
+            _need_cuda(Y, "Y", (torch.float32,))
+            M, K = X.shape
+            N = packed.shape[0]
+            if packed.shape[1] * 4 != K or tuple(Y.shape) != (M, N):
+                raise ValueError("forward_batch: shapes of X, packed and Y do not match")
+            d.X, d.x_dtype, d.M, d.K, d.N = _ptr(X), _x_dtype(X), M, K, N
+            d.packed, d.s_w, d.Y, d.acc = _ptr(packed), _ptr(s_w), _ptr(Y), _ptr(acc)
+    nb = workspace_bytes(BL_OP_FORWARD_BATCH, 0, 0, 0)
+    ws = _workspace(workspace, nb)
+    check(_lib.lib().bitlinear_forward_batch(descs, len(descs), eps, _ptr(ws), ws.numel(), _stream(stream)),
+          "bitlinear_forward_batch")
+    return descs
 
 
 def forward_q8(q: torch.Tensor, m: torch.Tensor, packed: torch.Tensor, s_w: torch.Tensor, return_acc: bool = False,

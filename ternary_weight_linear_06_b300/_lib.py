@@ -27,6 +27,15 @@ BL_STATIC_SCRATCH_BYTES = 8 << 20
 BL_OP_PACK = 0
 BL_OP_FORWARD = 1
 BL_OP_FFN = 2
+BL_OP_FORWARD_BATCH = 3
+BL_MAX_BATCH = 128
+
+
+class ForwardDesc(ctypes.Structure):
+    """Mirror of bl_forward_desc in include/bitlinear.h."""
+    _fields_ = [("X", ctypes.c_void_p), ("x_dtype", ctypes.c_int), ("M", ctypes.c_int), ("K", ctypes.c_int),
+                ("N", ctypes.c_int), ("packed", ctypes.c_void_p), ("s_w", ctypes.c_void_p),
+                ("Y", ctypes.c_void_p), ("acc", ctypes.c_void_p)]
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 
@@ -38,6 +47,7 @@ SIGNATURES = {
     "bitlinear_pack": (_i, [_vp, _i, _i, _f, _vp, _vp, _vp, _sz, _vp]),
     "bitlinear_quant_act": (_i, [_vp, _i, _i, _i, _f, _vp, _vp, _vp]),
     "bitlinear_forward": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp, _sz, _vp]),
+    "bitlinear_forward_batch": (_i, [ctypes.POINTER(ForwardDesc), _i, _f, _vp, _sz, _vp]),
     "bitlinear_forward_q8": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "bitlinear_forward_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp]),
     "bitlinear_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),

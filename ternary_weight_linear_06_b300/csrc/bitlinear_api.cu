@@ -80,10 +80,17 @@ T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
-// One BitLinear on an already-quantized input (int8 row-major q, scales m).
-bl_status run_linear(const int8_t* q, const float* m, int M, int K, const uint8_t* packed, const float* s_w, int N,
-                     float* Y, int32_t* acc, Epi epi, float* absmax_out, cudaStream_t st) {
-  return from_cuda(launch_gemv(packed, N, K, q, m, s_w, M, Y, acc, epi, absmax_out, true, st));
+GemvProblem make_problem(int M, int K, const uint8_t* packed, const float* s_w, int N, float* Y, int32_t* acc) {
+  GemvProblem p = {};
+  p.Wp = packed;
+  p.s_w = s_w;
+  p.N = N;
+  p.K = K;
+  p.M = M;
+  p.Y = Y;
+  p.acc = acc;
+  p.epi = Epi::kPlain;
+  return p;
 }
 
 bl_status check_linear_args(int M, int K, const uint8_t* packed, const float* s_w, int N, const float* Y,
@@ -129,6 +136,8 @@ size_t bitlinear_workspace_bytes(int op, int M, int N, int K) {
     case BL_OP_FORWARD:
       if (M < 0 || !valid_nk(N, K)) return 0;
       return fwd_layout(M, K).total;
+    case BL_OP_FORWARD_BATCH:
+      return sizeof(WsHeader);
     case BL_OP_FFN:
       if (M < 0 || !valid_nk(N, K) || !valid_k(N) || N == 0) return 0;
       return ffn_layout(M, K, N).total;
@@ -170,13 +179,41 @@ bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K, const uint
   if (!aligned16(X)) return BL_ERR_ALIGN;
   if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
     return s;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FwdLayout L = fwd_layout(M, K);
-  int8_t* q = at<int8_t>(workspace, L.q);
-  float* m = at<float>(workspace, L.m);
-  if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, true, st) != cudaSuccess)
-    return BL_ERR_CUDA;
-  return run_linear(q, m, M, K, packed, s_w, N, Y, acc, Epi::kPlain, nullptr, st);
+  GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
+  p.X = X;
+  p.x_dtype = x_dtype;
+  p.eps = eps;
+  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
+}
+
+bl_status bitlinear_forward_batch(const bl_forward_desc* descs, int count, float eps, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (count < 0 || count > BL_MAX_BATCH || !valid_eps(eps)) return BL_ERR_ARG;
+  if (count == 0) return BL_OK;
+  if (!descs || !workspace) return BL_ERR_ARG;
+  if (!aligned16(workspace)) return BL_ERR_ALIGN;
+  if (workspace_bytes < sizeof(WsHeader)) return BL_ERR_WORKSPACE;
+  GemvProblem ps[BL_MAX_BATCH];
+  int n = 0;
+  for (int i = 0; i < count; ++i) {
+    const bl_forward_desc& d = descs[i];
+    if (!valid_dtype(d.x_dtype)) return BL_ERR_ARG;
+    if (d.M < 0 || !valid_nk(d.N, d.K)) return BL_ERR_SHAPE;
+    if (d.M == 0 || d.N == 0) continue;
+    if (!d.X || !d.packed || !d.s_w || !d.Y) return BL_ERR_ARG;
+    if (!aligned16(d.X) || !aligned16(d.packed) || !aligned16(d.Y) || (d.acc && !aligned16(d.acc)) ||
+        (reinterpret_cast<uintptr_t>(d.s_w) & 3u))
+      return BL_ERR_ALIGN;
+    GemvProblem p = make_problem(d.M, d.K, d.packed, d.s_w, d.N, d.Y, d.acc);
+    p.X = d.X;
+    p.x_dtype = d.x_dtype;
+    p.eps = eps;
+    ps[n++] = p;
+  }
+  if (n == 0) return BL_OK;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  return from_cuda(launch_gemv_batch(ps, n, static_cast<WsHeader*>(workspace), true,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, const uint8_t* packed, const float* s_w,
@@ -188,7 +225,10 @@ bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, co
   if (!aligned16(q) || (reinterpret_cast<uintptr_t>(m) & 3u)) return BL_ERR_ALIGN;
   if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
     return s;
-  return run_linear(q, m, M, K, packed, s_w, N, Y, acc, Epi::kPlain, nullptr, static_cast<cudaStream_t>(stream));
+  GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
+  p.q = q;
+  p.m = m;
+  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
 }
 
 bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
@@ -205,21 +245,18 @@ bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t*
   if (bl_status s = check_device(); s != BL_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const FfnLayout L = ffn_layout(M, D, F);
-  int8_t* qx = at<int8_t>(workspace, L.qx);
-  float* mx = at<float>(workspace, L.mx);
   float* h = at<float>(workspace, L.h);
-  float* hmax = at<float>(workspace, L.hmax);
-  int8_t* qh = at<int8_t>(workspace, L.qh);
-  float* mh = at<float>(workspace, L.mh);
-  cudaError_t e = cudaMemsetAsync(hmax, 0, 4 * static_cast<size_t>(M), st);
-  if (e != cudaSuccess) return BL_ERR_CUDA;
-  e = launch_quant(X, x_dtype, M, D, eps, QLayout::kRowMajorI8, qx, mx, nullptr, nullptr, false, st);
-  if (e != cudaSuccess) return BL_ERR_CUDA;
-  bl_status s = run_linear(qx, mx, M, D, up, s_up, F, h, nullptr, Epi::kRelu2, hmax, st);
-  if (s != BL_OK) return s;
-  e = launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kRowMajorI8, qh, mh, nullptr, hmax, true, st);
-  if (e != cudaSuccess) return BL_ERR_CUDA;
-  return run_linear(qh, mh, M, F, down, s_down, D, Y, nullptr, Epi::kPlain, nullptr, st);
+  GemvProblem pu = make_problem(M, D, up, s_up, F, h, nullptr);
+  pu.X = X;
+  pu.x_dtype = x_dtype;
+  pu.eps = eps;
+  pu.epi = Epi::kRelu2;
+  if (launch_gemv(pu, static_cast<WsHeader*>(workspace), true, st) != cudaSuccess) return BL_ERR_CUDA;
+  GemvProblem pd = make_problem(M, F, down, s_down, D, Y, nullptr);
+  pd.X = h;
+  pd.x_dtype = BL_DTYPE_F32;
+  pd.eps = eps;
+  return from_cuda(launch_gemv(pd, static_cast<WsHeader*>(workspace), true, st));
 }
 
 bl_status bitlinear_unpack(const uint8_t* packed, int N, int K, int8_t* t, void* stream) {

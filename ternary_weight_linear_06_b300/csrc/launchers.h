@@ -31,11 +31,26 @@ cudaError_t launch_quant(const void* X, int x_dtype, int M, int K, float eps, QL
 
 // ----- decode GEMV (dp4a) ----------------------------------------------------
 enum class Epi : int { kPlain = 0, kRelu2 = 1 };
-// q: int8 row-major [M][K], m [M]. Writes Y [M][N] fp32 (or h = relu2(y) for kRelu2)
-// and optionally acc [M][N] int32. absmax_out (kRelu2 only, may be null):
-// per-row max of h, combined with atomicMax on the float bits (h >= 0).
-cudaError_t launch_gemv(const uint8_t* Wp, int N, int K, const int8_t* q, const float* m,
-                        const float* s_w, int M, float* Y, int32_t* acc,
-                        Epi epi, float* absmax_out, bool pdl, cudaStream_t st);
+struct GemvProblem {
+  const uint8_t* Wp;     // packed [N][K/4]
+  const float* s_w;      // [1]
+  int N, K, M;
+  // input: either X (fp32/bf16 [M][K], quantized inside the kernel with eps)
+  // or q (int8 row-major [M][K]) with its scales m [M]
+  const void* X;
+  int x_dtype;
+  float eps;
+  const int8_t* q;
+  const float* m;
+  float* Y;              // [M][N] fp32 (h = relu2(y) for kRelu2)
+  int32_t* acc;          // [M][N] or null
+  Epi epi;
+  float* absmax_out;     // kRelu2: per-row max of h via atomicMax on the bits, or null
+};
+constexpr int kGemvMaxBatch = 128;
+// One problem (M <= 4 per launch; more tokens take several launches).
+cudaError_t launch_gemv(const GemvProblem& p, WsHeader* status, bool pdl, cudaStream_t st);
+// Independent problems in one launch (count <= kGemvMaxBatch).
+cudaError_t launch_gemv_batch(const GemvProblem* ps, int count, WsHeader* status, bool pdl, cudaStream_t st);
 
 }  // namespace bl

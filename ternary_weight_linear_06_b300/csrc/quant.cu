@@ -18,43 +18,6 @@ namespace {
 
 constexpr int kThreads = 256;
 
-template <int DT>
-__device__ __forceinline__ void load16(const void* row, int g, float (&v)[16]) {
-  if constexpr (DT == BL_DTYPE_F32) {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(row) + 16 * g);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 u = __ldg(p + i);
-      v[4 * i + 0] = __uint_as_float(u.x);
-      v[4 * i + 1] = __uint_as_float(u.y);
-      v[4 * i + 2] = __uint_as_float(u.z);
-      v[4 * i + 3] = __uint_as_float(u.w);
-    }
-  } else {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(row) + 16 * g);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const uint4 u = __ldg(p + i);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[8 * i + 2 * j + 0] = __uint_as_float(w[j] << 16);          // exact bf16 -> fp32
-        v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-  return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
-         ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
-}
-
-__device__ __forceinline__ uint32_t pack_h2(int lo, int hi) {
-  const __half2 h = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 template <int DT, int LAYOUT>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict__ X, int K, float eps,
                                                          void* __restrict__ qout, float* __restrict__ m_out,

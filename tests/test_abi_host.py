@@ -81,3 +81,25 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_batch_argument_checks():
+    lib = _lib.lib()
+    buf = ctypes.create_string_buffer(4096 + 16)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    D = _lib.ForwardDesc
+    good = D(p, 0, 1, 64, 4, p, p, p, None)
+    arr = (D * 2)(good, good)
+    assert lib.bitlinear_forward_batch(arr, 129, 1e-5, p, 4096, None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_forward_batch(arr, -1, 1e-5, p, 4096, None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_forward_batch(arr, 0, 1e-5, p, 4096, None) == _lib.BL_OK
+    assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 16, None) == _lib.BL_ERR_WORKSPACE
+    arr[1].K = 96
+    assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 4096, None) == _lib.BL_ERR_SHAPE
+    arr[1].K = 64
+    arr[1].Y = p + 4
+    assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 4096, None) == _lib.BL_ERR_ALIGN
+    arr[1].Y = p
+    arr[1].x_dtype = 5
+    assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 4096, None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_workspace_bytes(_lib.BL_OP_FORWARD_BATCH, 0, 0, 0) == 256

@@ -198,3 +198,67 @@ def test_forward_q8_shared_quantization():
         assert_y(host(Y), O.dequant(acc_ref, s_ref, m_ref))
         Y2 = BL.forward(dev(X), packed, s_w)
         np.testing.assert_array_equal(host(Y2), host(Y))
+
+
+# ------------------------------------------------------------------- batch
+def _batch_case(specs, seed):
+    """specs: list of (M, K, N, bf16, want_acc). Returns problems + oracle refs."""
+    rng = np.random.default_rng(seed)
+    probs, refs = [], []
+    for i, (M, K, N, bf16, want_acc) in enumerate(specs):
+        W = WL.gaussian_weights(N, K, 0.02, seed=seed * 100 + i, outlier_frac=0.001)
+        packed, s_w, t_ref, s_ref = check_pack(W)
+        if bf16:
+            xb = WL.batched_activations_bf16(M, K, seed=seed * 100 + 50 + i)
+            Xd = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+            Xf = O.bf16_bits_to_f32(xb)
+        else:
+            Xf = WL.student_t(M, K, seed=seed * 100 + 50 + i) * np.float32(rng.uniform(0.1, 10))
+            Xd = dev(Xf)
+        Y = torch.full((M, N), float("nan"), device="cuda")
+        acc = torch.zeros((M, N), dtype=torch.int32, device="cuda") if want_acc else None
+        probs.append((Xd, packed, s_w, Y, acc) if want_acc else (Xd, packed, s_w, Y))
+        refs.append(O.forward(Xf, t_ref, s_ref))
+    return probs, refs
+
+
+def _check_batch(probs, refs):
+    for prob, (Y_ref, acc_ref, _, _) in zip(probs, refs):
+        assert_y(host(prob[3]), Y_ref)
+        if len(prob) > 4:
+            np.testing.assert_array_equal(host(prob[4]), acc_ref)
+
+
+def test_forward_batch_mixed_problems():
+    specs = [(1, 2560, 640, False, True), (1, 2560, 2560, False, False), (2, 320, 203, True, True),
+             (3, 6912, 100, False, True), (5, 128, 64, False, True), (1, 64, 7, True, True),
+             (4, 2048, 513, False, True), (0, 256, 16, False, False)]
+    probs, refs = _batch_case(specs, seed=3)
+    BL.forward_batch(probs)
+    _check_batch(probs, refs)
+
+
+def test_forward_batch_many_tiny_problems_next_to_a_large_one():
+    # byte-balanced CTA runs put the tiny problems together; the launch plan
+    # must split the batch when one run would touch too many problems
+    specs = [(1, 4096, 2048, False, True)] + [(1, 64, 4, False, True)] * 60 + [(2, 128, 12, True, True)] * 20
+    probs, refs = _batch_case(specs, seed=4)
+    BL.forward_batch(probs)
+    _check_batch(probs, refs)
+
+
+def test_forward_batch_matches_single_calls_bitwise():
+    specs = [(1, 2560, 640, False, True), (1, 6912, 256, False, True), (2, 2560, 96, False, True)]
+    probs, _ = _batch_case(specs, seed=5)
+    BL.forward_batch(probs)
+    for X, packed, s_w, Y, acc in probs:
+        Y1, acc1 = BL.forward(X, packed, s_w, return_acc=True)
+        np.testing.assert_array_equal(host(Y1).view(np.uint32), host(Y).view(np.uint32))
+        np.testing.assert_array_equal(host(acc1), host(acc))
+
+
+def test_forward_long_k_and_tiny_n():
+    for (M, K, N) in [(1, 65536, 8), (3, 65536, 5), (2, 16384, 4), (1, 28672, 130)]:
+        W = WL.gaussian_weights(N, K, 0.01, seed=K + N)
+        X = WL.student_t(M, K, seed=K + N + 1)
+        check_forward(W, X)
