@@ -5,8 +5,9 @@ projections of a 2B-class layer (q/o 2560->2560, k/v 2560->640, FFN up
 2560->6912, FFN down 6912->2560) for 30 independent layers: 120 independent
 problems, each with its own weights and its own input row. One step = the 120
 BitLinear forwards (per-token int8 quantization, packed ternary GEMV, dequant),
-issued as one bitlinear_forward_batch call (one persistent launch), captured
-once in a CUDA graph and replayed. The packed weights of one step (327 MB)
+issued as one bitlinear_forward_batch call (one quantization launch for all
+120 inputs, then one GEMV launch over all 120 weight matrices), captured once
+in a CUDA graph and replayed. The packed weights of one step (327 MB)
 exceed the 126 MB L2, so no flush is needed between steps. Metric: GB/s of
 packed weights streamed. The same 120 forwards issued as dependent
 bitlinear_forward calls (each waits for the previous one, as consecutive
@@ -135,6 +136,22 @@ def build_decode(torch, BL, WL, layers: int, device):
     return mats
 
 
+# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
+# capture summarised in profiles/gemv_batch_decode_m1_x12.md (12 layers). They
+# hold only for the kernel source they were taken on: a changed gemv.cu gives
+# traffic = null until it is profiled again.
+TRAFFIC = {"source": "ternary_weight_linear_06_b300/csrc/gemv.cu", "sha256_prefix": "b36f1b9887bb0ba1",
+           "bytes": 136.65e6, "layers": 12}
+
+
+def traffic_per_launch(layers: int):
+    import hashlib
+    with open(os.path.join(ROOT, TRAFFIC["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != TRAFFIC["sha256_prefix"]:
+            return None
+    return TRAFFIC["bytes"] * layers / TRAFFIC["layers"]
+
+
 def packed_bytes(mats):
     return sum(m["N"] * m["K"] // 4 for m in mats)
 
@@ -179,7 +196,7 @@ def run_ours(args):
     problems = [(m["X"], m["packed"], m["s_w"], m["Y"]) for m in mats]
 
     # ---- the step: the 120 independent forwards of one decode token in one
-    #      bitlinear_forward_batch call (one persistent GEMV launch)
+    #      bitlinear_forward_batch call (quantization launch + GEMV launch)
     with torch.cuda.stream(stream):
         descs = BL.forward_batch(problems, workspace=ws)        # first call outside capture
     torch.cuda.synchronize()
@@ -204,6 +221,19 @@ def run_ours(args):
     gc = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gc, stream=stream):
         chained()
+    torch.cuda.synchronize()
+
+    # ---- the GEMV alone (the dominant kernel): the same 120 problems given
+    #      already quantized, so the call launches only the GEMV
+    qms = [BL.quant_act(m["X"]) for m in mats]
+    y_q8 = [torch.empty_like(m["Y"]) for m in mats]
+    problems_q8 = [(q, m["packed"], m["s_w"], y, None, mm) for (q, mm), m, y in zip(qms, mats, y_q8)]
+    with torch.cuda.stream(stream):
+        descs_q8 = BL.forward_batch(problems_q8, workspace=ws)
+    torch.cuda.synchronize()
+    gq = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gq, stream=stream):
+        BL.forward_batch(problems_q8, workspace=ws, descs=descs_q8)
     torch.cuda.synchronize()
 
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[local_rank]
@@ -237,11 +267,15 @@ def run_ours(args):
     elapsed_max = float(t.item())
     clk = clocks.stop()
 
-    # dominant kernel: the step is one gemv_kernel launch, so its average
-    # launch duration is the timed region over the steps
-    launch_s = elapsed / args.steps
+    # dominant kernel: the GEMV launch alone, timed on the launching stream
+    with torch.cuda.stream(stream):
+        gemv_s = time_graph(torch, gq, args.steps, args.warmup, stream)
+    launch_s = gemv_s / args.steps
     alg_bytes_launch = gemv_algorithmic_bytes(mats)
     achieved = alg_bytes_launch / launch_s / 1e9
+    same = all(torch.equal(a["Y"], b) for a, b in zip(mats, y_q8))
+    traffic = traffic_per_launch(args.layers)
+    traffic = round(traffic) if traffic is not None else None
 
     chained_steps = max(20, args.steps // 5)
     with torch.cuda.stream(stream):
@@ -285,20 +319,24 @@ def run_ours(args):
                                f"down 6912x2560) x {args.layers} layers", "M": 1, "layers": args.layers,
                    "forwards_per_step": len(mats), "packed_bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2 (packed weights per step exceed 126 MB)",
-                   "launch": "one bitlinear_forward_batch call per step (120 independent problems), CUDA graph",
+                   "launch": "one bitlinear_forward_batch call per step (120 independent problems: one "
+                             "quantization launch + one GEMV launch), CUDA graph",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel (M=1, 120 problems per launch)",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                     "peak_source": f"{peak_src} hbm_gbs", "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "alg_bytes_per_launch": round(alg_bytes_launch), "avg_launch_us": round(launch_s * 1e6, 3)},
+                     "peak_source": f"{peak_src} hbm_gbs (burst copy)", "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "traffic_source": "ncu capture of 12 layers scaled by layers (profiles/gemv_batch_decode_m1_x12.md)",
+                     "alg_bytes_per_launch": round(alg_bytes_launch), "avg_launch_us": round(launch_s * 1e6, 3),
+                     "how": "the GEMV launch alone (the 120 problems given pre-quantized, one graph per step), "
+                            "CUDA events on the launching stream", "matches_step_output": same},
         "chained": {"value": round(bytes_step * chained_steps / chained_s / 1e9, 2), "unit": UNIT,
                     "ms_per_step": round(chained_s / chained_steps * 1e3, 4), "launches_per_step": len(mats),
                     "how": "the same 120 forwards as dependent bitlinear_forward calls in stream order "
                            "(programmatic dependent launch), CUDA graph"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host X -> device, graph replay, device Y -> pinned host, every step"},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -75,13 +75,18 @@ typedef enum {
   BL_ERR_WORKSPACE = 7     /* workspace smaller than bitlinear_workspace_bytes()     */
 } bl_status;
 
-typedef enum { BL_DTYPE_F32 = 0, BL_DTYPE_BF16 = 1 } bl_dtype;
+typedef enum {
+  BL_DTYPE_F32 = 0,
+  BL_DTYPE_BF16 = 1,
+  BL_DTYPE_I8 = 2      /* already quantized (int8 + per-token scale); bl_forward_desc only */
+} bl_dtype;
 
 typedef enum {
   BL_OP_PACK = 0,          /* bitlinear_pack(N, K)                          */
   BL_OP_FORWARD = 1,       /* bitlinear_forward(M, N, K)                    */
   BL_OP_FFN = 2,           /* bitlinear_ffn(M, N = F (hidden), K = D (model)) */
-  BL_OP_FORWARD_BATCH = 3  /* bitlinear_forward_batch (sizes ignored)       */
+  BL_OP_FORWARD_BATCH = 3  /* bitlinear_forward_batch(M = total tokens of all
+                              problems, K = their largest K, N ignored)      */
 } bl_op;
 
 /* Version of this ABI (major * 100 + minor). */
@@ -138,8 +143,8 @@ BL_API bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K,
  * bitlinear_forward call (all pointers on the device).
  */
 typedef struct {
-  const void* X;            /* [M, K] fp32 or bf16                       */
-  int x_dtype;              /* BL_DTYPE_F32 or BL_DTYPE_BF16             */
+  const void* X;            /* [M, K] fp32, bf16, or int8 (BL_DTYPE_I8)  */
+  int x_dtype;              /* BL_DTYPE_F32, BL_DTYPE_BF16 or BL_DTYPE_I8 */
   int M;                    /* tokens (>= 0)                             */
   int K;                    /* input features                            */
   int N;                    /* output features (>= 0)                    */
@@ -147,6 +152,8 @@ typedef struct {
   const float* s_w;         /* [1]                                       */
   float* Y;                 /* [M, N] output                             */
   int32_t* acc;             /* [M, N] int32 output, or NULL              */
+  const float* m;           /* BL_DTYPE_I8 only: [M] per-token scales as
+                               written by bitlinear_quant_act; else NULL */
 } bl_forward_desc;
 
 #define BL_MAX_BATCH 128
@@ -155,12 +162,15 @@ typedef struct {
  * `count` independent BitLinear forwards in one launch sequence (e.g. the
  * q, k and v projections of a layer, or the projections of several
  * independent sequences): each result equals that of bitlinear_forward on
- * the same arguments. No problem may read another's outputs. The packed
- * weights of all problems stream through one persistent grid, so small
- * matrices do not each pay a launch and a pipeline ramp.
+ * the same arguments (or of bitlinear_forward_q8 for BL_DTYPE_I8 inputs).
+ * No problem may read another's outputs. One kernel quantizes the inputs of
+ * all problems, then the packed weights of all problems stream through one
+ * grid, so small matrices do not each pay a launch and a pipeline ramp.
  *   descs     host array of `count` descriptors (0 <= count <= BL_MAX_BATCH),
  *             read during the call only.
- *   workspace >= bitlinear_workspace_bytes(BL_OP_FORWARD_BATCH, 0, 0, 0) bytes.
+ *   workspace >= bitlinear_workspace_bytes(BL_OP_FORWARD_BATCH, sum of M, 0,
+ *             largest K) bytes (the quantized activations of every problem;
+ *             problems given as BL_DTYPE_I8 need none).
  * Each descriptor is checked like bitlinear_forward's arguments; the first
  * failing check is returned and nothing is launched.
  */

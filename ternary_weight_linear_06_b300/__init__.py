@@ -14,7 +14,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_MAX_BATCH, BL_OP_FFN, BL_OP_FORWARD,  # noqa: F401
+from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_DTYPE_I8, BL_MAX_BATCH, BL_OP_FFN, BL_OP_FORWARD,  # noqa: F401
                    BL_OP_FORWARD_BATCH, BL_OP_PACK, BitLinearError, ForwardDesc, check)
 
 EPS = 1e-5
@@ -126,9 +126,11 @@ def forward(X: torch.Tensor, packed: torch.Tensor, s_w: torch.Tensor, eps: float
 
 def forward_batch(problems, eps: float = EPS, workspace: Workspace | None = None, stream=None, descs=None):
     """Independent BitLinear forwards in one call. `problems` is a sequence of
-    (X, packed, s_w, Y) or (X, packed, s_w, Y, acc) with device tensors; the
-    outputs Y (and acc) are written in place. Returns the ctypes descriptor
-    array, which can be passed back as `descs` to skip rebuilding it."""
+    (X, packed, s_w, Y), (X, packed, s_w, Y, acc) or (q, packed, s_w, Y, acc, m)
+    with device tensors: X fp32/bf16, or q int8 already quantized with its
+    per-token scales m (acc may be None). The outputs Y (and acc) are written in
+    place. Returns the ctypes descriptor array, which can be passed back as
+    `descs` to skip rebuilding it."""
     if descs is None:
         if len(problems) > BL_MAX_BATCH:
             raise ValueError(f"at most {BL_MAX_BATCH} problems per call")
@@ -136,16 +138,26 @@ def forward_batch(problems, eps: float = EPS, workspace: Workspace | None = None
         for d, prob in zip(descs, problems):
             X, packed, s_w, Y = prob[:4]
             acc = prob[4] if len(prob) > 4 else None
-            _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+            m = prob[5] if len(prob) > 5 else None
+            _need_cuda(X, "X", (torch.float32, torch.bfloat16, torch.int8))
             _need_cuda(packed, "packed", (torch.uint8,))
             _need_cuda(Y, "Y", (torch.float32,))
             M, K = X.shape
             N = packed.shape[0]
             if packed.shape[1] * 4 != K or tuple(Y.shape) != (M, N):
                 raise ValueError("forward_batch: shapes of X, packed and Y do not match")
-            d.X, d.x_dtype, d.M, d.K, d.N = _ptr(X), _x_dtype(X), M, K, N
+            if X.dtype == torch.int8:
+                if m is None:
+                    raise ValueError("forward_batch: an int8 input needs its per-token scales m")
+                _need_cuda(m, "m", (torch.float32,))
+                d.x_dtype, d.m = BL_DTYPE_I8, _ptr(m)
+            else:
+                d.x_dtype, d.m = _x_dtype(X), None
+            d.X, d.M, d.K, d.N = _ptr(X), M, K, N
             d.packed, d.s_w, d.Y, d.acc = _ptr(packed), _ptr(s_w), _ptr(Y), _ptr(acc)
-    nb = workspace_bytes(BL_OP_FORWARD_BATCH, 0, 0, 0)
+    tokens = sum(int(d.M) for d in descs if d.x_dtype != BL_DTYPE_I8)
+    kmax = max((int(d.K) for d in descs), default=64)
+    nb = workspace_bytes(BL_OP_FORWARD_BATCH, tokens, 0, kmax)
     ws = _workspace(workspace, nb)
     check(_lib.lib().bitlinear_forward_batch(descs, len(descs), eps, _ptr(ws), ws.numel(), _stream(stream)),
           "bitlinear_forward_batch")

@@ -21,6 +21,7 @@ BL_ERR_WORKSPACE = 7
 
 BL_DTYPE_F32 = 0
 BL_DTYPE_BF16 = 1
+BL_DTYPE_I8 = 2
 
 BL_STATIC_SCRATCH_BYTES = 8 << 20
 
@@ -35,7 +36,7 @@ class ForwardDesc(ctypes.Structure):
     """Mirror of bl_forward_desc in include/bitlinear.h."""
     _fields_ = [("X", ctypes.c_void_p), ("x_dtype", ctypes.c_int), ("M", ctypes.c_int), ("K", ctypes.c_int),
                 ("N", ctypes.c_int), ("packed", ctypes.c_void_p), ("s_w", ctypes.c_void_p),
-                ("Y", ctypes.c_void_p), ("acc", ctypes.c_void_p)]
+                ("Y", ctypes.c_void_p), ("acc", ctypes.c_void_p), ("m", ctypes.c_void_p)]
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 

@@ -10,7 +10,7 @@
 namespace bl {
 namespace {
 
-constexpr int kAbiVersion = 100;
+constexpr int kAbiVersion = 101;
 
 // Per-device capability cache: 0 unknown, 1 compute capability 10.3, -1 other.
 std::atomic<int> g_dev_ok[64];
@@ -44,6 +44,7 @@ bool valid_dtype(int d) { return d == BL_DTYPE_F32 || d == BL_DTYPE_BF16; }
 bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
 
 // Forward workspace: header | q (M*K fp16 or int8) | m [M] | qsum [M]
+// Batch workspace: header | q of every problem (M_p * K_p int8 each) | m of every problem
 struct FwdLayout {
   size_t q, m, qsum, total;
 };
@@ -136,8 +137,10 @@ size_t bitlinear_workspace_bytes(int op, int M, int N, int K) {
     case BL_OP_FORWARD:
       if (M < 0 || !valid_nk(N, K)) return 0;
       return fwd_layout(M, K).total;
-    case BL_OP_FORWARD_BATCH:
-      return sizeof(WsHeader);
+    case BL_OP_FORWARD_BATCH:     // M = total tokens of the batch, K = the largest K
+      if (M < 0 || (M > 0 && !valid_k(K))) return 0;
+      return sizeof(WsHeader) + align_up(static_cast<size_t>(M) * (M > 0 ? K : 0), 256) +
+             align_up(4 * static_cast<size_t>(M), 256);
     case BL_OP_FFN:
       if (M < 0 || !valid_nk(N, K) || !valid_k(N) || N == 0) return 0;
       return ffn_layout(M, K, N).total;
@@ -179,11 +182,16 @@ bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K, const uint
   if (!aligned16(X)) return BL_ERR_ALIGN;
   if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
     return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FwdLayout L = fwd_layout(M, K);
+  int8_t* q = at<int8_t>(workspace, L.q);
+  float* m = at<float>(workspace, L.m);
+  if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, true, st) != cudaSuccess)
+    return BL_ERR_CUDA;
   GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
-  p.X = X;
-  p.x_dtype = x_dtype;
-  p.eps = eps;
-  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
+  p.q = q;
+  p.m = m;
+  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));
 }
 
 bl_status bitlinear_forward_batch(const bl_forward_desc* descs, int count, float eps, void* workspace,
@@ -194,26 +202,51 @@ bl_status bitlinear_forward_batch(const bl_forward_desc* descs, int count, float
   if (!aligned16(workspace)) return BL_ERR_ALIGN;
   if (workspace_bytes < sizeof(WsHeader)) return BL_ERR_WORKSPACE;
   GemvProblem ps[BL_MAX_BATCH];
-  int n = 0;
+  QuantProblem qs[BL_MAX_BATCH];
+  int qidx[BL_MAX_BATCH];
+  int n = 0, nq = 0;
+  size_t q_bytes = 0, tokens = 0;
   for (int i = 0; i < count; ++i) {
     const bl_forward_desc& d = descs[i];
-    if (!valid_dtype(d.x_dtype)) return BL_ERR_ARG;
+    const bool pre = d.x_dtype == BL_DTYPE_I8;
+    if (!valid_dtype(d.x_dtype) && !pre) return BL_ERR_ARG;
+    if (pre && d.M > 0 && d.N > 0 && !d.m) return BL_ERR_ARG;
     if (d.M < 0 || !valid_nk(d.N, d.K)) return BL_ERR_SHAPE;
     if (d.M == 0 || d.N == 0) continue;
     if (!d.X || !d.packed || !d.s_w || !d.Y) return BL_ERR_ARG;
     if (!aligned16(d.X) || !aligned16(d.packed) || !aligned16(d.Y) || (d.acc && !aligned16(d.acc)) ||
         (reinterpret_cast<uintptr_t>(d.s_w) & 3u))
       return BL_ERR_ALIGN;
-    GemvProblem p = make_problem(d.M, d.K, d.packed, d.s_w, d.N, d.Y, d.acc);
-    p.X = d.X;
-    p.x_dtype = d.x_dtype;
-    p.eps = eps;
-    ps[n++] = p;
+    if (pre && (reinterpret_cast<uintptr_t>(d.m) & 3u)) return BL_ERR_ALIGN;
+    ps[n] = make_problem(d.M, d.K, d.packed, d.s_w, d.N, d.Y, d.acc);
+    if (pre) {
+      ps[n].q = static_cast<const int8_t*>(d.X);
+      ps[n].m = d.m;
+    } else {
+      qs[nq] = QuantProblem{d.X, d.x_dtype, d.M, d.K, nullptr, nullptr};
+      qidx[nq++] = n;
+      q_bytes += static_cast<size_t>(d.M) * d.K;
+      tokens += static_cast<size_t>(d.M);
+    }
+    ++n;
   }
   if (n == 0) return BL_OK;
+  // layout: header | q of problem 0, 1, ... | m of problem 0, 1, ...
+  const size_t m_off = sizeof(WsHeader) + align_up(q_bytes, 256);
+  if (workspace_bytes < m_off + align_up(4 * tokens, 256)) return BL_ERR_WORKSPACE;
   if (bl_status s = check_device(); s != BL_OK) return s;
-  return from_cuda(launch_gemv_batch(ps, n, static_cast<WsHeader*>(workspace), true,
-                                     static_cast<cudaStream_t>(stream)));
+  size_t qo = sizeof(WsHeader), mo = m_off;
+  for (int i = 0; i < nq; ++i) {
+    qs[i].q = at<int8_t>(workspace, qo);
+    qs[i].m = at<float>(workspace, mo);
+    ps[qidx[i]].q = qs[i].q;
+    ps[qidx[i]].m = qs[i].m;
+    qo += static_cast<size_t>(qs[i].M) * qs[i].K;
+    mo += 4 * static_cast<size_t>(qs[i].M);
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (nq > 0 && launch_quant_batch(qs, nq, eps, true, st) != cudaSuccess) return BL_ERR_CUDA;
+  return from_cuda(launch_gemv_batch(ps, n, static_cast<WsHeader*>(workspace), true, st));
 }
 
 bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, const uint8_t* packed, const float* s_w,
@@ -245,17 +278,24 @@ bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t*
   if (bl_status s = check_device(); s != BL_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const FfnLayout L = ffn_layout(M, D, F);
+  int8_t* qx = at<int8_t>(workspace, L.qx);
+  float* mx = at<float>(workspace, L.mx);
   float* h = at<float>(workspace, L.h);
+  int8_t* qh = at<int8_t>(workspace, L.qh);
+  float* mh = at<float>(workspace, L.mh);
+  if (launch_quant(X, x_dtype, M, D, eps, QLayout::kRowMajorI8, qx, mx, nullptr, nullptr, true, st) != cudaSuccess)
+    return BL_ERR_CUDA;
   GemvProblem pu = make_problem(M, D, up, s_up, F, h, nullptr);
-  pu.X = X;
-  pu.x_dtype = x_dtype;
-  pu.eps = eps;
+  pu.q = qx;
+  pu.m = mx;
   pu.epi = Epi::kRelu2;
   if (launch_gemv(pu, static_cast<WsHeader*>(workspace), true, st) != cudaSuccess) return BL_ERR_CUDA;
+  if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kRowMajorI8, qh, mh, nullptr, nullptr, true, st) !=
+      cudaSuccess)
+    return BL_ERR_CUDA;
   GemvProblem pd = make_problem(M, F, down, s_down, D, Y, nullptr);
-  pd.X = h;
-  pd.x_dtype = BL_DTYPE_F32;
-  pd.eps = eps;
+  pd.q = qh;
+  pd.m = mh;
   return from_cuda(launch_gemv(pd, static_cast<WsHeader*>(workspace), true, st));
 }
 

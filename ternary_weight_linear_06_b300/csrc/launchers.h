@@ -29,23 +29,28 @@ cudaError_t launch_quant(const void* X, int x_dtype, int M, int K, float eps, QL
                          void* q, float* m_out, int32_t* qsum_out, const float* absmax_in,
                          bool pdl, cudaStream_t st);
 
+// Row-major int8 quantization of several problems in one launch.
+struct QuantProblem {
+  const void* X;         // [M][K] fp32 or bf16
+  int x_dtype;
+  int M, K;
+  int8_t* q;             // [M][K] int8 out
+  float* m;              // [M] out
+};
+constexpr int kQuantMaxBatch = 128;
+cudaError_t launch_quant_batch(const QuantProblem* ps, int count, float eps, bool pdl, cudaStream_t st);
+
 // ----- decode GEMV (dp4a) ----------------------------------------------------
 enum class Epi : int { kPlain = 0, kRelu2 = 1 };
 struct GemvProblem {
   const uint8_t* Wp;     // packed [N][K/4]
   const float* s_w;      // [1]
   int N, K, M;
-  // input: either X (fp32/bf16 [M][K], quantized inside the kernel with eps)
-  // or q (int8 row-major [M][K]) with its scales m [M]
-  const void* X;
-  int x_dtype;
-  float eps;
-  const int8_t* q;
-  const float* m;
+  const int8_t* q;       // int8 activations, row-major [M][K]
+  const float* m;        // their per-token scales [M]
   float* Y;              // [M][N] fp32 (h = relu2(y) for kRelu2)
   int32_t* acc;          // [M][N] or null
   Epi epi;
-  float* absmax_out;     // kRelu2: per-row max of h via atomicMax on the bits, or null
 };
 constexpr int kGemvMaxBatch = 128;
 // One problem (M <= 4 per launch; more tokens take several launches).

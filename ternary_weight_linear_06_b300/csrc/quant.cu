@@ -8,8 +8,9 @@
 // One CTA per token row: pass 1 reduces |x| to the row absmax (skipped when
 // the caller supplies it), pass 2 quantizes 16 columns per thread step and
 // writes them in the layout the consumer wants (row-major int8, or fp16 in
-// the tensor-core operand order), plus sum_k q_k when asked (the matmul
-// kernels multiply by the stored code t + 1 and subtract it).
+// the tensor-core operand order), plus sum_k q_k when asked. A batched
+// variant quantizes the token rows of up to kQuantMaxBatch problems in one
+// launch.
 #include "common.cuh"
 #include "launchers.h"
 
@@ -18,23 +19,16 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Quantize one token row (all threads of the CTA take part).
 template <int DT, int LAYOUT>
-__global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict__ X, int K, float eps,
-                                                         void* __restrict__ qout, float* __restrict__ m_out,
-                                                         int32_t* __restrict__ qsum_out,
-                                                         const float* __restrict__ absmax_in) {
-  __shared__ float s_red[kThreads / 32];
-  __shared__ int s_sum[kThreads / 32];
-  pdl_wait();
-  const int row = blockIdx.x;
+__device__ __forceinline__ void quant_row(const void* __restrict__ xr, int K, float eps, void* __restrict__ qout_row,
+                                          float* __restrict__ m_out, int32_t* __restrict__ qsum_out,
+                                          const float* __restrict__ absmax_in, float* s_red, int* s_sum) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t esize = DT == BL_DTYPE_F32 ? 4 : 2;
-  const void* xr = static_cast<const char*>(X) + static_cast<size_t>(row) * K * esize;
   const int G = K >> 4;
-
   float amax;
   if (absmax_in != nullptr) {
-    amax = absmax_in[row];
+    amax = *absmax_in;
   } else {
     float a = 0.0f;
     for (int g = tid; g < G; g += kThreads) {
@@ -66,17 +60,16 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict_
     if constexpr (LAYOUT == static_cast<int>(QLayout::kRowMajorI8)) {
       uint4 o = make_uint4(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]),
                            pack4(q[8], q[9], q[10], q[11]), pack4(q[12], q[13], q[14], q[15]));
-      reinterpret_cast<uint4*>(static_cast<int8_t*>(qout) + static_cast<size_t>(row) * K)[g] = o;
+      reinterpret_cast<uint4*>(qout_row)[g] = o;
     } else {
       // fp16 slot s holds column (s >> 1) + 8 * (s & 1)
       uint4 o0 = make_uint4(pack_h2(q[0], q[8]), pack_h2(q[1], q[9]), pack_h2(q[2], q[10]), pack_h2(q[3], q[11]));
       uint4 o1 = make_uint4(pack_h2(q[4], q[12]), pack_h2(q[5], q[13]), pack_h2(q[6], q[14]), pack_h2(q[7], q[15]));
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(qout) + static_cast<size_t>(row) * K) + 2 * g;
+      uint4* dst = reinterpret_cast<uint4*>(qout_row) + 2 * g;
       dst[0] = o0;
       dst[1] = o1;
     }
   }
-  pdl_trigger();
   if (qsum_out != nullptr) {
     qs = warp_sum(qs);
     if (lane == 0) s_sum[warp] = qs;
@@ -85,10 +78,60 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict_
       int t = 0;
 #pragma unroll
       for (int w = 0; w < kThreads / 32; ++w) t += s_sum[w];
-      qsum_out[row] = t;
+      *qsum_out = t;
     }
   }
-  if (tid == 0 && m_out != nullptr) m_out[row] = m;
+  if (tid == 0 && m_out != nullptr) *m_out = m;
+}
+
+template <int DT, int LAYOUT>
+__global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict__ X, int K, float eps,
+                                                         void* __restrict__ qout, float* __restrict__ m_out,
+                                                         int32_t* __restrict__ qsum_out,
+                                                         const float* __restrict__ absmax_in) {
+  __shared__ float s_red[kThreads / 32];
+  __shared__ int s_sum[kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int row = blockIdx.x;
+  const size_t esize = DT == BL_DTYPE_F32 ? 4 : 2;
+  const size_t qsize = LAYOUT == static_cast<int>(QLayout::kRowMajorI8) ? 1 : 2;
+  quant_row<DT, LAYOUT>(static_cast<const char*>(X) + static_cast<size_t>(row) * K * esize, K, eps,
+                        static_cast<char*>(qout) + static_cast<size_t>(row) * K * qsize,
+                        m_out != nullptr ? m_out + row : nullptr, qsum_out != nullptr ? qsum_out + row : nullptr,
+                        absmax_in != nullptr ? absmax_in + row : nullptr, s_red, s_sum);
+}
+
+// Row-major int8 quantization of the token rows of several problems in one
+// launch: CTA b quantizes row b of the concatenated rows.
+struct QuantBatchArgs {
+  QuantProblem prob[kQuantMaxBatch];
+  int row_begin[kQuantMaxBatch + 1];
+  int count;
+  float eps;
+};
+
+__global__ void __launch_bounds__(kThreads) quant_batch_kernel(const __grid_constant__ QuantBatchArgs a) {
+  __shared__ float s_red[kThreads / 32];
+  __shared__ int s_sum[kThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x;
+  int lo = 0, hi = a.count - 1;             // problem p with row_begin[p] <= b < row_begin[p+1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.row_begin[mid] <= b) lo = mid;
+    else hi = mid - 1;
+  }
+  const QuantProblem& P = a.prob[lo];
+  const int row = b - a.row_begin[lo];
+  const size_t esize = P.x_dtype == BL_DTYPE_F32 ? 4 : 2;
+  const void* xr = static_cast<const char*>(P.X) + static_cast<size_t>(row) * P.K * esize;
+  int8_t* qr = P.q + static_cast<size_t>(row) * P.K;
+  if (P.x_dtype == BL_DTYPE_F32)
+    quant_row<BL_DTYPE_F32, 0>(xr, P.K, a.eps, qr, P.m + row, nullptr, nullptr, s_red, s_sum);
+  else
+    quant_row<BL_DTYPE_BF16, 0>(xr, P.K, a.eps, qr, P.m + row, nullptr, nullptr, s_red, s_sum);
 }
 
 template <int DT, int LAYOUT>
@@ -107,6 +150,32 @@ cudaError_t launch_t(const void* X, int M, int K, float eps, void* q, float* m_o
 }
 
 }  // namespace
+
+cudaError_t launch_quant_batch(const QuantProblem* ps, int count, float eps, bool pdl, cudaStream_t st) {
+  QuantBatchArgs a;
+  int rows = 0, n = 0;
+  for (int i = 0; i < count; ++i) {
+    if (ps[i].M <= 0) continue;
+    a.prob[n] = ps[i];
+    a.row_begin[n] = rows;
+    rows += ps[i].M;
+    ++n;
+  }
+  if (n == 0) return cudaSuccess;
+  a.row_begin[n] = rows;
+  a.count = n;
+  a.eps = eps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(rows));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, quant_batch_kernel, a);
+}
 
 cudaError_t launch_quant(const void* X, int x_dtype, int M, int K, float eps, QLayout layout, void* q,
                          float* m_out, int32_t* qsum_out, const float* absmax_in, bool pdl, cudaStream_t st) {

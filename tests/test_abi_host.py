@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     lib = _lib.lib()
-    assert lib.bitlinear_version() == 100
+    assert lib.bitlinear_version() == 101
     for s in range(8):
         assert lib.bitlinear_status_str(s)
     assert b"unknown" in lib.bitlinear_status_str(99)
@@ -102,4 +102,9 @@ def test_batch_argument_checks():
     arr[1].Y = p
     arr[1].x_dtype = 5
     assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 4096, None) == _lib.BL_ERR_ARG
+    # an already-quantized input needs its per-token scales
+    arr[1].x_dtype = _lib.BL_DTYPE_I8
+    assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 4096, None) == _lib.BL_ERR_ARG
+    arr[1].m = p + 2
+    assert lib.bitlinear_forward_batch(arr, 2, 1e-5, p, 4096, None) == _lib.BL_ERR_ALIGN
     assert lib.bitlinear_workspace_bytes(_lib.BL_OP_FORWARD_BATCH, 0, 0, 0) == 256

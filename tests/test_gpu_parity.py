@@ -257,6 +257,21 @@ def test_forward_batch_matches_single_calls_bitwise():
         np.testing.assert_array_equal(host(acc1), host(acc))
 
 
+def test_forward_batch_prequantized_inputs():
+    # BL_DTYPE_I8 problems (int8 + per-token scales) next to fp32 and bf16 ones
+    specs = [(1, 2560, 640, False, True), (3, 6912, 256, True, True), (2, 2560, 96, False, True)]
+    probs, refs = _batch_case(specs, seed=7)
+    mixed = []
+    for i, (X, packed, s_w, Y, acc) in enumerate(probs):
+        if i != 1:
+            q, m = BL.quant_act(X)
+            mixed.append((q, packed, s_w, Y, acc, m))
+        else:
+            mixed.append((X, packed, s_w, Y, acc))
+    BL.forward_batch(mixed)
+    _check_batch(probs, refs)
+
+
 def test_forward_long_k_and_tiny_n():
     for (M, K, N) in [(1, 65536, 8), (3, 65536, 5), (2, 16384, 4), (1, 28672, 130)]:
         W = WL.gaussian_weights(N, K, 0.01, seed=K + N)
