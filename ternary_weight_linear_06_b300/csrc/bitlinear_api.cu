@@ -1,6 +1,6 @@
 // C ABI of the BitLinear library: argument checks, workspace layout and the
 // launch sequence of each call. The kernels live in pack.cu, quant.cu,
-// gemv.cu and gemm_tc.cu.
+// gemv.cu (decode, fewer than kGemmMinTokens tokens) and gemm_tc.cu (more).
 #include <atomic>
 #include <cmath>
 
@@ -94,6 +94,22 @@ GemvProblem make_problem(int M, int K, const uint8_t* packed, const float* s_w, 
   return p;
 }
 
+GemmProblem make_gemm(int M, int K, const uint8_t* packed, const float* s_w, int N, const void* act, const float* m,
+                      float* Y, int32_t* acc, bool relu2) {
+  GemmProblem g = {};
+  g.Wp = packed;
+  g.s_w = s_w;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.act = act;
+  g.m = m;
+  g.Y = Y;
+  g.acc = acc;
+  g.relu2 = relu2;
+  return g;
+}
+
 bl_status check_linear_args(int M, int K, const uint8_t* packed, const float* s_w, int N, const float* Y,
                             const int32_t* acc, void* workspace, size_t workspace_bytes) {
   if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
@@ -184,8 +200,16 @@ bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K, const uint
     return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const FwdLayout L = fwd_layout(M, K);
-  int8_t* q = at<int8_t>(workspace, L.q);
   float* m = at<float>(workspace, L.m);
+  if (M >= kGemmMinTokens) {
+    // prefill: fp16 activations in the tensor-core order, then the tcgen05 GEMM
+    void* act = at<void>(workspace, L.q);
+    if (launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, nullptr, nullptr, true, st) != cudaSuccess)
+      return BL_ERR_CUDA;
+    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false),
+                                 static_cast<WsHeader*>(workspace), true, st));
+  }
+  int8_t* q = at<int8_t>(workspace, L.q);
   if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, true, st) != cudaSuccess)
     return BL_ERR_CUDA;
   GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
@@ -258,10 +282,17 @@ bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, co
   if (!aligned16(q) || (reinterpret_cast<uintptr_t>(m) & 3u)) return BL_ERR_ALIGN;
   if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
     return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M >= kGemmMinTokens) {
+    void* act = at<void>(workspace, fwd_layout(M, K).q);
+    if (launch_widen_pair(q, M, K, act, true, st) != cudaSuccess) return BL_ERR_CUDA;
+    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false),
+                                 static_cast<WsHeader*>(workspace), true, st));
+  }
   GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
   p.q = q;
   p.m = m;
-  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));
 }
 
 bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
@@ -278,6 +309,20 @@ bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t*
   if (bl_status s = check_device(); s != BL_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const FfnLayout L = ffn_layout(M, D, F);
+  if (M >= kGemmMinTokens) {
+    void* ax = at<void>(workspace, L.qx);
+    float* mx = at<float>(workspace, L.mx);
+    float* h = at<float>(workspace, L.h);
+    void* ah = at<void>(workspace, L.qh);
+    float* mh = at<float>(workspace, L.mh);
+    WsHeader* hdr = static_cast<WsHeader*>(workspace);
+    if (launch_quant(X, x_dtype, M, D, eps, QLayout::kPairF16, ax, mx, nullptr, nullptr, true, st) != cudaSuccess ||
+        launch_gemm(make_gemm(M, D, up, s_up, F, ax, mx, h, nullptr, true), hdr, true, st) != cudaSuccess ||
+        launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kPairF16, ah, mh, nullptr, nullptr, true, st) !=
+            cudaSuccess)
+      return BL_ERR_CUDA;
+    return from_cuda(launch_gemm(make_gemm(M, F, down, s_down, D, ah, mh, Y, nullptr, false), hdr, true, st));
+  }
   int8_t* qx = at<int8_t>(workspace, L.qx);
   float* mx = at<float>(workspace, L.mx);
   float* h = at<float>(workspace, L.h);

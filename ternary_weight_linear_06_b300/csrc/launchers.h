@@ -39,6 +39,8 @@ struct QuantProblem {
 };
 constexpr int kQuantMaxBatch = 128;
 cudaError_t launch_quant_batch(const QuantProblem* ps, int count, float eps, bool pdl, cudaStream_t st);
+// int8 row-major [M][K] -> fp16 [M][K] in the kPairF16 order.
+cudaError_t launch_widen_pair(const int8_t* q, int M, int K, void* out, bool pdl, cudaStream_t st);
 
 // ----- decode GEMV (dp4a) ----------------------------------------------------
 enum class Epi : int { kPlain = 0, kRelu2 = 1 };
@@ -57,5 +59,20 @@ constexpr int kGemvMaxBatch = 128;
 cudaError_t launch_gemv(const GemvProblem& p, WsHeader* status, bool pdl, cudaStream_t st);
 // Independent problems in one launch (count <= kGemvMaxBatch).
 cudaError_t launch_gemv_batch(const GemvProblem* ps, int count, WsHeader* status, bool pdl, cudaStream_t st);
+
+// ----- prefill / batched GEMM (tcgen05, TMEM, TMA) ---------------------------
+struct GemmProblem {
+  const uint8_t* Wp;     // packed [N][K/4]
+  const float* s_w;      // [1]
+  int M, N, K;
+  const void* act;       // fp16 [M][K] in the pair order (QLayout::kPairF16)
+  const float* m;        // [M] per-token scales
+  float* Y;              // [M][N]
+  int32_t* acc;          // [M][N] or null
+  bool relu2;            // FFN up: write h = relu(y)^2
+};
+// Tokens from which the forward takes the tensor-core GEMM instead of the GEMV.
+constexpr int kGemmMinTokens = 17;
+cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st);
 
 }  // namespace bl

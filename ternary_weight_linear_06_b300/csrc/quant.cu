@@ -149,7 +149,43 @@ cudaError_t launch_t(const void* X, int M, int K, float eps, void* q, float* m_o
   return cudaLaunchKernelEx(&cfg, quant_kernel<DT, LAYOUT>, X, K, eps, q, m_out, qsum_out, absmax_in);
 }
 
+// int8 row-major -> fp16 in the tensor-core pair order (an input quantized
+// elsewhere, given to the GEMM). One thread per 16-column group.
+__global__ void __launch_bounds__(256) widen_pair_kernel(const int8_t* __restrict__ q, size_t groups,
+                                                         uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t g = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += stride) {
+    const uint4 v = reinterpret_cast<const uint4*>(q)[g];
+    int b[16];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) b[i] = static_cast<int>(static_cast<int8_t>((w[i >> 2] >> (8 * (i & 3))) & 0xFFu));
+    out[2 * g] = make_uint4(pack_h2(b[0], b[8]), pack_h2(b[1], b[9]), pack_h2(b[2], b[10]), pack_h2(b[3], b[11]));
+    out[2 * g + 1] = make_uint4(pack_h2(b[4], b[12]), pack_h2(b[5], b[13]), pack_h2(b[6], b[14]), pack_h2(b[7], b[15]));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_widen_pair(const int8_t* q, int M, int K, void* out, bool pdl, cudaStream_t st) {
+  const size_t groups = static_cast<size_t>(M) * K / 16;
+  if (groups == 0) return cudaSuccess;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>((groups + 255) / 256, static_cast<size_t>(8 * sms)));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, widen_pair_kernel, q, groups, static_cast<uint4*>(out));
+}
 
 cudaError_t launch_quant_batch(const QuantProblem* ps, int count, float eps, bool pdl, cudaStream_t st) {
   QuantBatchArgs a;

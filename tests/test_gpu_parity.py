@@ -277,3 +277,87 @@ def test_forward_long_k_and_tiny_n():
         W = WL.gaussian_weights(N, K, 0.01, seed=K + N)
         X = WL.student_t(M, K, seed=K + N + 1)
         check_forward(W, X)
+
+
+# ------------------------------------------------- tensor-core GEMM (M >= 17)
+@pytest.mark.parametrize("M,K,N", [(17, 64, 128), (64, 320, 203), (128, 2560, 640), (129, 576, 130),
+                                   (300, 2560, 257), (1000, 128, 384)])
+def test_gemm_path_ragged_tiles(M, K, N):
+    # several 128-token and 128-row tiles with ragged tails, K from one to 40 steps
+    W = WL.gaussian_weights(N, K, 0.02, seed=M + K + N, outlier_frac=0.001)
+    X = WL.prefill_activations(M, K, seed=M * 7 + K)
+    X[min(3, M - 1)] = 0.0
+    check_forward(W, X)
+
+
+def test_gemm_path_bf16_batched_decode_inputs():
+    W = WL.decode_weights("up", 0)
+    xb = WL.batched_activations_bf16(64, 2560, seed=78)
+    check_forward(W, xb, x_is_bf16_bits=True)
+
+
+def test_gemm_exact_at_the_accumulator_bound():
+    # every q = 127 and every t = +1 at K = 65536: acc = 127 * 65536 = 8,323,072 (< 2^24)
+    M, K, N = 20, 65536, 16
+    W = np.full((N, K), 0.5, np.float32)
+    W[1::2] = -0.5                                     # alternate rows all -1
+    X = np.ones((M, K), np.float32)
+    X[1] = -1.0
+    packed, s_w, t_ref, s_ref = check_pack(W)
+    Y, acc = BL.forward(dev(X), packed, s_w, return_acc=True)
+    Y_ref, acc_ref, _, _ = O.forward(X, t_ref, s_ref)
+    assert acc_ref[0, 0] == 127 * K and acc_ref[0, 1] == -127 * K
+    np.testing.assert_array_equal(host(acc), acc_ref)
+    assert_y(host(Y), Y_ref)
+
+
+def test_gemm_exact_large_plus_small_partial_sums():
+    # a large running sum followed by many +-1 contributions: truncating
+    # accumulation would lose the small terms
+    M, K, N = 32, 16384, 64
+    rng = np.random.default_rng(5)
+    X = np.empty((M, K), np.float32)
+    X[:, : K // 2] = 127.0                             # q = 127 on the first half
+    X[:, K // 2:] = rng.choice([-1.0, 1.0], size=(M, K // 2)).astype(np.float32)   # q = +-1 after scaling
+    W = rng.choice([-0.5, 0.0, 0.5], size=(N, K)).astype(np.float32)
+    W[:, : K // 2] = 0.5
+    check_forward(W, X)
+
+
+def test_gemm_ffn_prefill_block():
+    D, F, M = 256, 640, 200
+    Wu = WL.gaussian_weights(F, D, 0.02, seed=93, outlier_frac=0.001)
+    Wd = WL.gaussian_weights(D, F, 0.02, seed=94, outlier_frac=0.001)
+    X = WL.prefill_activations(M, D, seed=95)
+    up, s_up = BL.pack(dev(Wu))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sd, td = O.pack_weights(Wd)
+    Y = BL.ffn(dev(X), up, s_up, down, s_down)
+    Y_ref, _ = O.ffn(X, tu, su, td, sd)
+    assert_y(host(Y), Y_ref)
+
+
+def test_gemm_forward_q8_prequantized():
+    M, K, N = 96, 2560, 640
+    X = WL.prefill_activations(M, K, seed=97)
+    W = WL.decode_weights("kv", 4)
+    q, m = BL.quant_act(dev(X))
+    packed, s_w, t_ref, s_ref = check_pack(W)
+    Y, acc = BL.forward_q8(q, m, packed, s_w, return_acc=True)
+    q_ref, m_ref = O.quant_act(X)
+    acc_ref = O.int_matmul(q_ref, t_ref)
+    np.testing.assert_array_equal(host(acc), acc_ref)
+    assert_y(host(Y), O.dequant(acc_ref, s_ref, m_ref))
+
+
+def test_gemm_and_gemv_agree_bitwise_across_the_switch():
+    # the same token rows through the GEMV (4 tokens) and the GEMM (all tokens)
+    W = WL.decode_weights("qo", 6)
+    X = WL.student_t(40, 2560, seed=98)
+    packed, s_w = BL.pack(dev(W))
+    Y_all, acc_all = BL.forward(dev(X), packed, s_w, return_acc=True)
+    Y_few, acc_few = BL.forward(dev(X[:4]), packed, s_w, return_acc=True)
+    np.testing.assert_array_equal(host(acc_all)[:4], host(acc_few))
+    np.testing.assert_array_equal(host(Y_all)[:4].view(np.uint32), host(Y_few).view(np.uint32))
+    assert BL.workspace_status() == 0
