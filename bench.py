@@ -309,6 +309,7 @@ def run_ours(args):
     e2e_value = bytes_step * e_steps / e2e_s / 1e9 * world
 
     assert BL.workspace_status(ws) == 0, "device-side status word set"
+    prefill = None if args.no_prefill else prefill_leg(torch, BL, WL, device, peaks, peak_src, stream)
 
     value = bytes_step * args.steps * world / elapsed_max / 1e9
     out = {
@@ -337,6 +338,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host X -> device, graph replay, device Y -> pinned host, every step"},
         "gpu_launches": 2 * args.steps,
+        "prefill": prefill,
         "clocks": clk,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -346,6 +348,80 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(out))
+
+
+# --------------------------------------------------------- prefill leg
+def time_each(torch, fn, iters, stream, flush=None):
+    """Mean device time of fn() over iters calls, each bracketed by CUDA events
+    on `stream`; L2 is flushed (a write larger than L2) between calls."""
+    tot = 0.0
+    for _ in range(iters):
+        if flush is not None:
+            flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) / 1e3
+    return tot / iters
+
+
+def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096):
+    """Prefill: M tokens through the four 2B-class projections (forward =
+    quantization + tensor-core GEMM; and the GEMM alone on a pre-quantized
+    input) and through the fused FFN block 2560 -> 6912 -> ReLU^2 -> 2560."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = {"M": M, "unit": "TOPS", "forward": {}, "gemm_only": {}, "ms": {}}
+    ws = BL.Workspace(0, device)
+    best = None
+    with torch.cuda.stream(stream):
+        for shape in SHAPE_ORDER:
+            K, N = WL.SHAPES_2B[shape]
+            W = torch.from_numpy(WL.decode_weights(shape, 0)).to(device)
+            packed, s_w = BL.pack(W)
+            del W
+            X = torch.from_numpy(WL.prefill_activations(M, K, seed=9000 + K + N)).to(device)
+            Y = torch.empty((M, N), dtype=torch.float32, device=device)
+            act, m = BL.quant_act_tc(X)
+            BL.forward(X, packed, s_w, out=Y, workspace=ws)
+            BL.forward_tc(act, m, packed, s_w, out=Y, workspace=ws)
+            torch.cuda.synchronize()
+            ops = 2.0 * M * N * K
+            t_fwd = time_each(torch, lambda: BL.forward(X, packed, s_w, out=Y, workspace=ws), iters, stream, flush)
+            t_mm = time_each(torch, lambda: BL.forward_tc(act, m, packed, s_w, out=Y, workspace=ws), iters, stream,
+                             flush)
+            out["forward"][shape] = round(ops / t_fwd / 1e12, 1)
+            out["gemm_only"][shape] = round(ops / t_mm / 1e12, 1)
+            out["ms"][shape] = {"forward": round(t_fwd * 1e3, 4), "gemm": round(t_mm * 1e3, 4)}
+            if shape == "up":
+                best = (ops, t_mm)
+            del X, Y, act, m, packed
+        D, F = 2560, 6912
+        up, s_up = BL.pack(torch.from_numpy(WL.decode_weights("up", 1)).to(device))
+        down, s_down = BL.pack(torch.from_numpy(WL.decode_weights("down", 1)).to(device))
+        X = torch.from_numpy(WL.prefill_activations(M, D, seed=9100)).to(device)
+        Yf = torch.empty((M, D), dtype=torch.float32, device=device)
+        BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws)
+        torch.cuda.synchronize()
+        t_ffn = time_each(torch, lambda: BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws), iters, stream,
+                          flush)
+        out["ffn"] = round(4.0 * M * D * F / t_ffn / 1e12, 1)
+        out["ms"]["ffn"] = round(t_ffn * 1e3, 4)
+    ops, t_mm = best
+    achieved = ops / t_mm / 1e12
+    peak = peaks["bf16_tflops"]
+    out["roofline"] = {"bound": "tensor", "kernel": f"gemm_tc_kernel (FFN up 2560->6912, M={M})",
+                       "achieved": round(achieved, 1), "peak": peak,
+                       "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the same nominal dense rate)",
+                       "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                       "alg_ops_per_launch": ops, "avg_launch_us": round(t_mm * 1e6, 2),
+                       "how": "one bitlinear_forward_tc launch per timed call (CUDA events on the launching "
+                              "stream), L2 flushed between calls"}
+    out["how"] = ("integer-valued fp16 operands on tcgen05 kind::f16 (sm_103a has no int8 tcgen05 MMA); "
+                  "ops = 2*M*N*K per projection, 4*M*D*F for the FFN")
+    return out
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -428,6 +504,7 @@ def main():
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (M=4096) leg")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -190,6 +190,31 @@ BL_API bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, in
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Per-token absmax quantization ("BitNet解读", 激活量化) into the operand form
+ * of the tensor-core contraction: the same int8 values q as
+ * bitlinear_quant_act, stored as fp16 [M, K] (exact: |q| <= 128), with the
+ * columns of every 16-column group in the order 0, 8, 1, 9, ..., 7, 15.
+ *   act      [M, K] fp16 (2 bytes per element), device, output, 16-byte aligned.
+ *   m        [M] fp32, device, output.
+ * Use it to quantize once and run several bitlinear_forward_tc calls.
+ */
+BL_API bl_status bitlinear_quant_act_tc(const void* X, int x_dtype, int M, int K, float eps, void* act, float* m,
+                                 void* stream);
+
+/*
+ * BitLinear forward on an input already in the tensor-core operand form
+ * (bitlinear_quant_act_tc): the tcgen05 contraction and the dequant epilogue
+ * only ("BitNet b1.58 2B4T Technical Report | Summary", 5.1: packed weights
+ * unpacked on chip and multiplied with 8-bit activations). Any M >= 0; the
+ * result equals bitlinear_forward on the unquantized input.
+ *   workspace >= 256 bytes (its status word; see bitlinear_workspace_status).
+ */
+BL_API bl_status bitlinear_forward_tc(const void* act, const float* m, int M, int K,
+                               const uint8_t* packed, const float* s_w, int N,
+                               float* Y, int32_t* acc,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Size of the fixed device scratch array behind bitlinear_forward_noalloc.
  */
 #define BL_STATIC_SCRATCH_BYTES (8u << 20)

@@ -19,7 +19,8 @@ from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_DTYPE_I8, BL_MAX_BATCH, BL_OP
 
 EPS = 1e-5
 
-__all__ = ["pack", "quant_act", "forward", "forward_batch", "forward_q8", "forward_noalloc", "ffn", "unpack", "workspace_bytes", "workspace_status",
+__all__ = ["pack", "quant_act", "quant_act_tc", "forward", "forward_batch", "forward_q8", "forward_tc",
+           "forward_noalloc", "ffn", "unpack", "workspace_bytes", "workspace_status",
            "Workspace", "BitLinearError", "EPS", "library_path"]
 
 
@@ -181,6 +182,38 @@ def forward_q8(q: torch.Tensor, m: torch.Tensor, packed: torch.Tensor, s_w: torc
     ws = _workspace(workspace, nb)
     check(_lib.lib().bitlinear_forward_q8(_ptr(q), _ptr(m), M, K, _ptr(packed), _ptr(s_w), N, _ptr(Y), _ptr(acc),
                                           _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_forward_q8")
+    return (Y, acc) if return_acc else Y
+
+
+def quant_act_tc(X: torch.Tensor, eps: float = EPS, stream=None):
+    """Per-token absmax quantization into the tensor-core operand form.
+    Returns (act fp16 [M, K], m fp32 [M]) for forward_tc."""
+    _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+    M, K = X.shape
+    act = torch.empty((M, K), dtype=torch.float16, device=X.device)
+    m = torch.empty(max(M, 4), dtype=torch.float32, device=X.device)[:M]
+    check(_lib.lib().bitlinear_quant_act_tc(_ptr(X), _x_dtype(X), M, K, eps, _ptr(act), _ptr(m), _stream(stream)),
+          "bitlinear_quant_act_tc")
+    return act, m
+
+
+def forward_tc(act: torch.Tensor, m: torch.Tensor, packed: torch.Tensor, s_w: torch.Tensor,
+               return_acc: bool = False, out: torch.Tensor | None = None, workspace: Workspace | None = None,
+               stream=None):
+    """BitLinear on an input from quant_act_tc: the tensor-core contraction only."""
+    _need_cuda(act, "act", (torch.float16,))
+    _need_cuda(m, "m", (torch.float32,))
+    _need_cuda(packed, "packed", (torch.uint8,))
+    _need_cuda(s_w, "s_w", (torch.float32,))
+    M, K = act.shape
+    N = packed.shape[0]
+    if packed.shape[1] * 4 != K:
+        raise ValueError(f"packed has {packed.shape[1]} bytes per row, expected K/4 = {K // 4}")
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=act.device)
+    acc = torch.empty((M, N), dtype=torch.int32, device=act.device) if return_acc else None
+    ws = _workspace(workspace, 256)
+    check(_lib.lib().bitlinear_forward_tc(_ptr(act), _ptr(m), M, K, _ptr(packed), _ptr(s_w), N, _ptr(Y), _ptr(acc),
+                                          _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_forward_tc")
     return (Y, acc) if return_acc else Y
 
 

@@ -50,6 +50,8 @@ SIGNATURES = {
     "bitlinear_forward": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp, _sz, _vp]),
     "bitlinear_forward_batch": (_i, [ctypes.POINTER(ForwardDesc), _i, _f, _vp, _sz, _vp]),
     "bitlinear_forward_q8": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+    "bitlinear_quant_act_tc": (_i, [_vp, _i, _i, _i, _f, _vp, _vp, _vp]),
+    "bitlinear_forward_tc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "bitlinear_forward_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp]),
     "bitlinear_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "bitlinear_unpack": (_i, [_vp, _i, _i, _vp, _vp]),

@@ -295,6 +295,33 @@ bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, co
   return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));
 }
 
+bl_status bitlinear_quant_act_tc(const void* X, int x_dtype, int M, int K, float eps, void* act, float* m,
+                                 void* stream) {
+  if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
+  if (M < 0 || !valid_k(K)) return BL_ERR_SHAPE;
+  if (M == 0) return BL_OK;
+  if (!X || !act || !m) return BL_ERR_ARG;
+  if (!aligned16(X) || !aligned16(act) || (reinterpret_cast<uintptr_t>(m) & 3u)) return BL_ERR_ALIGN;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, nullptr, nullptr, false,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+bl_status bitlinear_forward_tc(const void* act, const float* m, int M, int K, const uint8_t* packed,
+                               const float* s_w, int N, float* Y, int32_t* acc, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
+  if (M == 0 || N == 0) return BL_OK;
+  if (!act || !m || !packed || !s_w || !Y || !workspace) return BL_ERR_ARG;
+  if (!aligned16(act) || !aligned16(packed) || !aligned16(Y) || !aligned16(workspace) || (acc && !aligned16(acc)) ||
+      (reinterpret_cast<uintptr_t>(m) & 3u) || (reinterpret_cast<uintptr_t>(s_w) & 3u))
+    return BL_ERR_ALIGN;
+  if (workspace_bytes < sizeof(WsHeader)) return BL_ERR_WORKSPACE;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false),
+                               static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
+}
+
 bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
                         const uint8_t* down, const float* s_down, int F, float eps, float* Y, void* workspace,
                         size_t workspace_bytes, void* stream) {

@@ -74,6 +74,12 @@ def test_host_argument_checks_fail_before_launch():
     assert lib.bitlinear_forward(None, 0, 3, 64, None, None, 0, 1e-5, None, None, None, 0, None) == _lib.BL_OK
     assert lib.bitlinear_quant_act(None, 0, 0, 64, 1e-5, None, None, None) == _lib.BL_OK
     assert lib.bitlinear_workspace_status(None, None) == _lib.BL_ERR_ARG
+    # tensor-core operand form
+    assert lib.bitlinear_quant_act_tc(p, 0, 2, 96, 1e-5, p, p, None) == _lib.BL_ERR_SHAPE
+    assert lib.bitlinear_quant_act_tc(p, 0, 2, 64, 1e-5, p + 8, p, None) == _lib.BL_ERR_ALIGN
+    assert lib.bitlinear_forward_tc(p, p, 2, 64, p, p, 4, p, None, p, 16, None) == _lib.BL_ERR_WORKSPACE
+    assert lib.bitlinear_forward_tc(p + 8, p, 2, 64, p, p, 4, p, None, p, 4096, None) == _lib.BL_ERR_ALIGN
+    assert lib.bitlinear_forward_tc(None, None, 0, 64, None, None, 4, None, None, None, 0, None) == _lib.BL_OK
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

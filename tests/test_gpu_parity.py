@@ -361,3 +361,21 @@ def test_gemm_and_gemv_agree_bitwise_across_the_switch():
     np.testing.assert_array_equal(host(acc_all)[:4], host(acc_few))
     np.testing.assert_array_equal(host(Y_all)[:4].view(np.uint32), host(Y_few).view(np.uint32))
     assert BL.workspace_status() == 0
+
+
+def test_forward_tc_matches_the_oracle_and_forward():
+    # the tensor-core operand form: quantize once, run the contraction only
+    for M, K, N in [(5, 2560, 640), (256, 6912, 257)]:
+        W = WL.gaussian_weights(N, K, 0.02, seed=K + N + M, outlier_frac=0.001)
+        X = WL.prefill_activations(M, K, seed=M + 99)
+        packed, s_w, t_ref, s_ref = check_pack(W)
+        act, m = BL.quant_act_tc(dev(X))
+        Y, acc = BL.forward_tc(act, m, packed, s_w, return_acc=True)
+        Y_ref, acc_ref, q_ref, m_ref = O.forward(X, t_ref, s_ref)
+        np.testing.assert_array_equal(host(act).astype(np.int32).reshape(M, K // 16, 8, 2).transpose(0, 1, 3, 2)
+                                      .reshape(M, K), q_ref)
+        np.testing.assert_array_equal(host(m).view(np.uint32), m_ref.view(np.uint32))
+        np.testing.assert_array_equal(host(acc), acc_ref)
+        assert_y(host(Y), Y_ref)
+        Y2 = BL.forward(dev(X), packed, s_w)
+        np.testing.assert_array_equal(host(Y2).view(np.uint32), host(Y).view(np.uint32))
