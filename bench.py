@@ -368,16 +368,16 @@ def time_each(torch, fn, iters, stream, flush=None):
     return tot / iters
 
 
-def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096):
+def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096, shapes=None, ffn=True):
     """Prefill: M tokens through the four 2B-class projections (forward =
     quantization + tensor-core GEMM; and the GEMM alone on a pre-quantized
     input) and through the fused FFN block 2560 -> 6912 -> ReLU^2 -> 2560."""
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     out = {"M": M, "unit": "TOPS", "forward": {}, "gemm_only": {}, "ms": {}}
     ws = BL.Workspace(0, device)
-    best = None
+    best, best_shape = None, None
     with torch.cuda.stream(stream):
-        for shape in SHAPE_ORDER:
+        for shape in (shapes or SHAPE_ORDER):
             K, N = WL.SHAPES_2B[shape]
             W = torch.from_numpy(WL.decode_weights(shape, 0)).to(device)
             packed, s_w = BL.pack(W)
@@ -395,24 +395,27 @@ def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096
             out["forward"][shape] = round(ops / t_fwd / 1e12, 1)
             out["gemm_only"][shape] = round(ops / t_mm / 1e12, 1)
             out["ms"][shape] = {"forward": round(t_fwd * 1e3, 4), "gemm": round(t_mm * 1e3, 4)}
-            if shape == "up":
-                best = (ops, t_mm)
+            if shape == "up" or best is None:
+                best, best_shape = (ops, t_mm), shape
             del X, Y, act, m, packed
+    if ffn:
         D, F = 2560, 6912
-        up, s_up = BL.pack(torch.from_numpy(WL.decode_weights("up", 1)).to(device))
-        down, s_down = BL.pack(torch.from_numpy(WL.decode_weights("down", 1)).to(device))
-        X = torch.from_numpy(WL.prefill_activations(M, D, seed=9100)).to(device)
-        Yf = torch.empty((M, D), dtype=torch.float32, device=device)
-        BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws)
-        torch.cuda.synchronize()
-        t_ffn = time_each(torch, lambda: BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws), iters, stream,
-                          flush)
+        with torch.cuda.stream(stream):
+            up, s_up = BL.pack(torch.from_numpy(WL.decode_weights("up", 1)).to(device))
+            down, s_down = BL.pack(torch.from_numpy(WL.decode_weights("down", 1)).to(device))
+            X = torch.from_numpy(WL.prefill_activations(M, D, seed=9100)).to(device)
+            Yf = torch.empty((M, D), dtype=torch.float32, device=device)
+            BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws)
+            torch.cuda.synchronize()
+            t_ffn = time_each(torch, lambda: BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws), iters,
+                              stream, flush)
         out["ffn"] = round(4.0 * M * D * F / t_ffn / 1e12, 1)
         out["ms"]["ffn"] = round(t_ffn * 1e3, 4)
     ops, t_mm = best
     achieved = ops / t_mm / 1e12
+    up_name = "FFN up 2560->6912" if best_shape == "up" else best_shape
     peak = peaks["bf16_tflops"]
-    out["roofline"] = {"bound": "tensor", "kernel": f"gemm_tc_kernel (FFN up 2560->6912, M={M})",
+    out["roofline"] = {"bound": "tensor", "kernel": f"gemm_tc_kernel ({up_name}, M={M})",
                        "achieved": round(achieved, 1), "peak": peak,
                        "peak_source": f"{peak_src} bf16_tflops (burst; fp16 has the same nominal dense rate)",
                        "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
@@ -495,6 +498,21 @@ def run_reference(args):
     print(json.dumps(out))
 
 
+def run_prefill_only(args):
+    import torch
+
+    import ternary_weight_linear_06_b300 as BL
+    from ternary_weight_linear_06_b300 import workloads as WL
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    peaks, peak_src = measured_peaks()
+    stream = torch.cuda.Stream(device)
+    shapes = [x for x in args.prefill_shapes.split(",") if x] or None
+    out = prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=args.prefill_iters, shapes=shapes,
+                      ffn=not args.prefill_no_ffn)
+    print(json.dumps(out))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -505,11 +523,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill (M=4096) leg")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill leg (profiling); prints its JSON object")
+    ap.add_argument("--prefill-iters", type=int, default=20)
+    ap.add_argument("--prefill-shapes", default="", help="comma-separated subset of qo,kv,up,down")
+    ap.add_argument("--prefill-no-ffn", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        run_prefill_only(args)
     else:
         run_ours(args)
 

@@ -14,20 +14,24 @@
 // the fp32 accumulation in TMEM is exact and acc = float(sum) holds the
 // integer result.
 //
-// Tile: 128 weight rows (the MMA's M) x 128 tokens (its N), K in steps of 64.
+// Tile: 128 weight rows (the MMA's M) x 128, 192 or 256 tokens (its N; the
+// host picks the width from the tile count, wider instructions run closer to
+// the tensor-core peak), K in steps of 64.
 //   * A (weights) lives in TMEM: converter warps read the 2-bit codes of their
 //     row (16 bytes per K step, staged by TMA), turn them into fp16 t values
 //     in registers and write them with tcgen05.st, so the expanded weights
 //     never take shared-memory bandwidth;
 //   * B (activations) is fp16 in shared memory, staged by TMA with the
 //     128-byte swizzle the MMA descriptor names;
-//   * D is two 128-column fp32 accumulators in TMEM, so the epilogue of one
-//     tile overlaps the MMAs of the next.
+//   * D is fp32 in TMEM: two accumulators for 128- and 192-token tiles, so the
+//     epilogue of one tile overlaps the MMAs of the next; one for 256-token
+//     tiles (TMEM has 512 columns, and the weight stages need some).
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer (one lane): activation tile + packed code tile per stage
 //   warp 1      MMA issuer (one lane); the warp owns the TMEM allocation
-//   warps 2-5   converters: packed codes -> fp16 t in TMEM (warp w owns TMEM lanes 32*(w%4)..)
-//   warps 6-9   epilogue: TMEM -> registers, y = fp32(acc * fp32(fp32(s_w*m)/127)), stores
+//   warps 2-9   converters: packed codes -> fp16 t in TMEM; warp w owns TMEM lanes
+//               32*(w%4).. and every other K step (two warps per lane quarter)
+//   warps 10-13 epilogue: TMEM -> registers, y = fp32(acc * fp32(fp32(s_w*m)/127)), stores
 // Every mbarrier wait is bounded: on a timeout the thread records
 // BL_ERR_TIMEOUT, raises the CTA's abort flag (which ends every other role's
 // waits), and the CTA drains its copies and MMAs (bounded) before it frees
@@ -50,18 +54,43 @@ namespace bl {
 namespace {
 
 constexpr int kTileN = 128;           // weight rows per tile (MMA M)
-constexpr int kTileM = 128;           // tokens per tile (MMA N)
 constexpr int kTileK = 64;            // K per stage: one 128-byte swizzle row of fp16
-constexpr int kStages = 6;
-constexpr int kThreads = 320;         // 10 warps
+constexpr int kConvWarps = 8;         // two per TMEM lane quarter, alternating K steps
+constexpr int kEpiWarp0 = 2 + kConvWarps;
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;   // 14 warps
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;       // accumulators: columns [0, 128) and [128, 256)
-constexpr uint32_t kACol = 256;       // A stages: 32 columns each
-constexpr uint32_t kBBytes = kTileM * kTileK * 2;   // 16 KB
-constexpr uint32_t kPBytes = kTileN * kTileK / 4;   // 2 KB
+constexpr uint32_t kPBytes = kTileN * kTileK / 4;   // 2 KB of codes per stage
 // at least this much dynamic shared memory, so that one CTA fits per SM and
 // no second CTA waits on the first one's TMEM
 constexpr size_t kMinSmem = 120 * 1024;
+
+// Tile shapes: TM tokens per tile (the MMA's N; one instruction covers all
+// of them, and wider instructions run closer to the tensor-core peak),
+// ST pipeline stages, NB accumulator buffers in TMEM (two let the epilogue of
+// one tile overlap the MMAs of the next). TMEM columns: NB * TM for the
+// accumulators, then ST * 32 for the weight stages.
+template <int TM, int ST, int NB>
+struct Cfg {
+  static constexpr int kTileM = TM;
+  static constexpr int kStages = ST;
+  static constexpr int kAccBufs = NB;
+  static constexpr uint32_t kAccCol = 0;
+  static constexpr uint32_t kACol = static_cast<uint32_t>(TM * NB);
+  static constexpr uint32_t kBBytes = TM * kTileK * 2;
+  static_assert(TM % 16 == 0 && TM >= 16 && TM <= 256, "MMA N must be a multiple of 16 in [16, 256]");
+  static_assert(kACol + ST * 32 <= kTmemCols, "accumulators and weight stages exceed TMEM");
+  static_assert(ST % 2 == 0, "converter parity split assumes an even stage count");
+  // Instruction descriptor: D fp32, A fp16, B fp16, both K-major, N = TM, M = kTileN.
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | (static_cast<uint32_t>(TM >> 3) << 17) | (static_cast<uint32_t>(kTileN >> 4) << 24);
+  static size_t smem_bytes() {
+    const size_t need = 1024 + ST * (kBBytes + kPBytes) + 256;
+    return need > kMinSmem ? need : kMinSmem;
+  }
+};
+using CfgWide = Cfg<256, 6, 1>;     // 256 tokens, one accumulator
+using CfgMid = Cfg<192, 4, 2>;      // 192 tokens, two accumulators
+using CfgNarrow = Cfg<128, 8, 2>;   // 128 tokens (few tokens), two accumulators
 
 struct GemmParams {
   int M, N, K;
@@ -73,10 +102,11 @@ struct GemmParams {
   WsHeader* status;
 };
 
+template <int ST>
 struct SmemCtl {
-  uint64_t full[kStages];      // TMA bytes of a stage landed
-  uint64_t aready[kStages];    // converters wrote the stage's A into TMEM
-  uint64_t empty[kStages];     // MMAs that read the stage are done
+  uint64_t full[ST];           // TMA bytes of a stage landed
+  uint64_t aready[ST];         // converters wrote the stage's A into TMEM
+  uint64_t empty[ST];          // MMAs that read the stage are done
   uint64_t accfull[2];         // accumulator b holds a finished tile
   uint64_t accempty[2];        // epilogue drained accumulator b
   uint64_t done;               // final commit of the MMA thread
@@ -103,15 +133,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor: D fp32, A fp16, B fp16, both K-major, N = kTileM, M = kTileN.
-constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kTileM >> 3) << 17) |
-                            (static_cast<uint32_t>(kTileN >> 4) << 24);
-
+template <uint32_t IDESC>
 __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "r"(a), "l"(bdesc), "n"(IDESC), "r"(accumulate)
       : "memory");
 }
 
@@ -155,7 +182,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   }
 }
 
-__device__ __forceinline__ void raise_abort(SmemCtl* ctl, WsHeader* status, uint32_t where) {
+template <typename Ctl>
+__device__ __forceinline__ void raise_abort(Ctl* ctl, WsHeader* status, uint32_t where) {
   if (atomicExch(&ctl->abort, 1) == 0) report_status(status, BL_ERR_TIMEOUT, where);
 }
 
@@ -172,15 +200,22 @@ __device__ __forceinline__ uint32_t pair_word(uint32_t w_lo, uint32_t w_hi) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                    const GemmParams p) {
+  constexpr int kTileM = C::kTileM;
+  constexpr int kStages = C::kStages;
+  constexpr uint32_t kBBytes = C::kBBytes;
+  constexpr uint32_t kAccCol = C::kAccCol;
+  constexpr uint32_t kACol = C::kACol;
+  using Ctl = SmemCtl<kStages>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled stages
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = smem;                                           // [kStages][kBBytes]
   uint8_t* sP = smem + kStages * kBBytes;                       // [kStages][kPBytes]
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(sP + kStages * kPBytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(sP + kStages * kPBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_n = (p.N + kTileN - 1) / kTileN;
@@ -257,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int local = 0;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
-        const int b = local & 1;
-        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        const int b = C::kAccBufs == 2 ? (local & 1) : 0;
+        const uint32_t use = static_cast<uint32_t>(C::kAccBufs == 2 ? (local >> 1) : local);
         if (!wait_or_abort(&ctl->accempty[b], (use & 1u) ^ 1u, deadline, abort_flag)) {
           raise_abort(ctl, p.status, 0x400u + blockIdx.x);
           break;
@@ -277,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = sw128_desc(smem_u32(sB + s * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)
-            mma_f16_tmem_a(d, a + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), (kt | kk) != 0 ? 1u : 0u);
+            mma_f16_tmem_a<C::kIdesc>(d, a + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), (kt | kk) != 0 ? 1u : 0u);
           mma_commit(&ctl->empty[s]);
           if (++s == kStages) {
             s = 0;
@@ -290,16 +325,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&ctl->done);
       (void)mbar_wait_until(&ctl->done, 0, global_ns() + kWaitLimitNs / 4);
     }
-  } else if (warp < 6) {
+  } else if (warp < kEpiWarp0) {
     // ---------------- converters: codes -> fp16 t in TMEM ----------------
     const int quarter = warp & 3;
+    const int parity = (warp - 2) >> 2;                  // this warp's K steps: step % 2 == parity
     const int row = quarter * 32 + lane;                 // row of the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    int step = 0;                                        // K steps of all tiles, in order
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      for (int kt = 0; kt < ktiles; ++kt) {
+      for (int kt = 0; kt < ktiles; ++kt, ++step) {
+        if ((step & 1) != parity) {
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1u;
+          }
+          continue;
+        }
         const bool got = wait_or_abort(&ctl->full[s], ph, deadline, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) raise_abort(ctl, p.status, 0x600u + blockIdx.x);
@@ -333,15 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue (warps kEpiWarp0 .. kEpiWarp0 + 3) ----------------
     const int quarter = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sw = p.s_w[0];
     int local = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
       const int tn = tile / tiles_m, tm = tile % tiles_m;
-      const int b = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      const int b = C::kAccBufs == 2 ? (local & 1) : 0;
+      const uint32_t use = static_cast<uint32_t>(C::kAccBufs == 2 ? (local >> 1) : local);
       const bool got = wait_or_abort(&ctl->accfull[b], use & 1u, deadline, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) raise_abort(ctl, p.status, 0x700u + blockIdx.x);
@@ -421,19 +465,13 @@ int sm_count() {
   return n > 0 ? n : 148;
 }
 
-}  // namespace
 
-size_t gemm_smem_bytes() {
-  const size_t need = 1024 + kStages * (kBBytes + kPBytes) + sizeof(SmemCtl);
-  return std::max(need, kMinSmem);
-}
-
-cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st) {
-  if (g.M == 0 || g.N == 0) return cudaSuccess;
+template <class C>
+cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st) {
   CUtensorMap tm_act, tm_codes;
   // activations: fp16 [M][K] (pair order within 16-column groups)
   if (!make_map_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.act, static_cast<uint64_t>(g.K),
-                   static_cast<uint64_t>(g.M), static_cast<uint64_t>(g.K) * 2, kTileK, kTileM,
+                   static_cast<uint64_t>(g.M), static_cast<uint64_t>(g.K) * 2, kTileK, C::kTileM,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // packed codes: uint8 [N][K/4]
@@ -451,11 +489,11 @@ cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaSt
   p.acc = g.acc;
   p.relu2 = g.relu2 ? 1 : 0;
   p.status = status;
-  const int tiles = ((g.N + kTileN - 1) / kTileN) * ((g.M + kTileM - 1) / kTileM);
+  const int tiles = ((g.N + kTileN - 1) / kTileN) * ((g.M + C::kTileM - 1) / C::kTileM);
   const int grid = std::max(1, std::min(tiles, sm_count()));
-  const size_t smem = gemm_smem_bytes();
-  cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  const size_t smem = C::smem_bytes();
+  auto kern = gemm_tc_kernel<C>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -467,7 +505,30 @@ cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaSt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tm_act, tm_codes, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_act, tm_codes, p);
+}
+
+// Estimated cost of a tile shape: rounds of persistent tiles over the SMs
+// times the tile's token count plus a fixed per-tile cost, with a small
+// penalty for a single accumulator (the epilogue then stalls the MMAs).
+double tile_cost(int M, int N, int tile_m, bool single_acc, int sms) {
+  const long long tiles = static_cast<long long>((N + kTileN - 1) / kTileN) * ((M + tile_m - 1) / tile_m);
+  const long long rounds = (tiles + sms - 1) / sms;
+  return static_cast<double>(rounds) * (tile_m + 32) * (single_acc ? 1.05 : 1.0);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  const int sms = sm_count();
+  if (g.M <= CfgNarrow::kTileM) return launch_cfg<CfgNarrow>(g, status, pdl, st);
+  const double wide = tile_cost(g.M, g.N, CfgWide::kTileM, true, sms);
+  const double mid = tile_cost(g.M, g.N, CfgMid::kTileM, false, sms);
+  const double narrow = tile_cost(g.M, g.N, CfgNarrow::kTileM, false, sms);
+  if (wide <= mid && wide <= narrow) return launch_cfg<CfgWide>(g, status, pdl, st);
+  if (mid <= narrow) return launch_cfg<CfgMid>(g, status, pdl, st);
+  return launch_cfg<CfgNarrow>(g, status, pdl, st);
 }
 
 }  // namespace bl

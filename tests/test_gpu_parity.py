@@ -379,3 +379,38 @@ def test_forward_tc_matches_the_oracle_and_forward():
         assert_y(host(Y), Y_ref)
         Y2 = BL.forward(dev(X), packed, s_w)
         np.testing.assert_array_equal(host(Y2).view(np.uint32), host(Y).view(np.uint32))
+
+
+# full-size prefill shapes: every tile shape of the GEMM (the host picks 256-,
+# 192- or 128-token tiles from the tile count), checked on sampled token rows
+def _sampled_rows(M, seed):
+    rng = np.random.default_rng(seed)
+    rows = {0, 1, M - 1, M - 2, M // 2}
+    for tile in (128, 192, 256):
+        rows.update(r for r in (tile - 1, tile, 3 * tile - 1, 3 * tile) if r < M)
+    rows.update(rng.choice(M, size=24, replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+def _check_sampled(W, X, seed):
+    M = X.shape[0]
+    packed, s_w = BL.pack(dev(W))
+    _, s_ref, t_ref = O.pack_weights(W)
+    Y, acc = BL.forward(dev(X), packed, s_w, return_acc=True)
+    rows = _sampled_rows(M, seed)
+    q_ref, m_ref = O.quant_act(X[rows])
+    acc_ref = (q_ref.astype(np.float64) @ t_ref.astype(np.float64).T).astype(np.int64)   # exact: |acc| < 2^53
+    np.testing.assert_array_equal(host(acc)[rows], acc_ref)
+    assert_y(host(Y)[rows], O.dequant(acc_ref, s_ref, m_ref))
+
+
+@pytest.mark.parametrize("shape", ["qo", "kv", "up", "down"])
+def test_gemm_full_size_prefill_sampled_rows(shape):
+    K, N = WL.SHAPES_2B[shape]
+    _check_sampled(WL.decode_weights(shape, 3), WL.prefill_activations(4096, K, seed=300 + K + N), 17)
+
+
+@pytest.mark.parametrize("M", [512, 2048])
+def test_gemm_70b_class_shape_sampled_rows(M):
+    K, N = 8192, 8192
+    _check_sampled(WL.gaussian_weights(N, K, 0.01, seed=M, outlier_frac=0.001), WL.student_t(M, K, seed=M + 1), 19)
