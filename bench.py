@@ -498,6 +498,50 @@ def run_reference(args):
     print(json.dumps(out))
 
 
+def run_crossover(args):
+    """Batched decode: GEMV (dp4a) vs tensor-core GEMM per shape and token count,
+    each call timed alone with L2 flushed between calls; the crossover is the
+    smallest M from which the GEMM is faster."""
+    import torch
+
+    import ternary_weight_linear_06_b300 as BL
+    from ternary_weight_linear_06_b300 import workloads as WL
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    ws = BL.Workspace(0, device)
+    Ms = [1, 2, 4, 8, 12, 16, 24, 32, 48, 64, 128, 256]
+    out = {"what": "batched decode: GEMV vs tensor-core GEMM (us per call, L2 flushed)", "M": Ms, "shapes": {}}
+    with torch.cuda.stream(stream):
+        for shape in SHAPE_ORDER:
+            K, N = WL.SHAPES_2B[shape]
+            packed, s_w = BL.pack(torch.from_numpy(WL.decode_weights(shape, 2)).to(device))
+            rows = {"gemv_us": [], "gemm_us": [], "crossover_M": None}
+            for M in Ms:
+                xb = WL.batched_activations_bf16(M, K, seed=700 + M)
+                X = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).to(device)
+                q, m = BL.quant_act(X)
+                act, m2 = BL.quant_act_tc(X)
+                Y1 = torch.empty((M, N), dtype=torch.float32, device=device)
+                Y2 = torch.empty((M, N), dtype=torch.float32, device=device)
+                prob = [(q, packed, s_w, Y1, None, m)]
+                descs = BL.forward_batch(prob, workspace=ws)
+                BL.forward_tc(act, m2, packed, s_w, out=Y2, workspace=ws)
+                torch.cuda.synchronize()
+                assert torch.equal(Y1, Y2), (shape, M)
+                t1 = time_each(torch, lambda: BL.forward_batch(prob, workspace=ws, descs=descs), args.prefill_iters,
+                               stream, flush)
+                t2 = time_each(torch, lambda: BL.forward_tc(act, m2, packed, s_w, out=Y2, workspace=ws),
+                               args.prefill_iters, stream, flush)
+                rows["gemv_us"].append(round(t1 * 1e6, 2))
+                rows["gemm_us"].append(round(t2 * 1e6, 2))
+                if rows["crossover_M"] is None and t2 < t1:
+                    rows["crossover_M"] = M
+            out["shapes"][shape] = rows
+    print(json.dumps(out))
+
+
 def run_prefill_only(args):
     import torch
 
@@ -528,6 +572,8 @@ def main():
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--prefill-shapes", default="", help="comma-separated subset of qo,kv,up,down")
     ap.add_argument("--prefill-no-ffn", action="store_true")
+    ap.add_argument("--crossover", action="store_true",
+                    help="batched decode GEMV vs GEMM sweep (prints its own JSON; not the bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -535,6 +581,8 @@ def main():
         run_reference(args)
     elif args.prefill_only:
         run_prefill_only(args)
+    elif args.crossover:
+        run_crossover(args)
     else:
         run_ours(args)
 

@@ -31,7 +31,8 @@
 //   warp 1      MMA issuer (one lane); the warp owns the TMEM allocation
 //   warps 2-9   converters: packed codes -> fp16 t in TMEM; warp w owns TMEM lanes
 //               32*(w%4).. and every other K step (two warps per lane quarter)
-//   warps 10-13 epilogue: TMEM -> registers, y = fp32(acc * fp32(fp32(s_w*m)/127)), stores
+//   warps 10-17 epilogue: TMEM -> registers, y = fp32(acc * fp32(fp32(s_w*m)/127)), stores;
+//               warp w owns TMEM lanes 32*(w%4).. and every other 32-token chunk
 // Every mbarrier wait is bounded: on a timeout the thread records
 // BL_ERR_TIMEOUT, raises the CTA's abort flag (which ends every other role's
 // waits), and the CTA drains its copies and MMAs (bounded) before it frees
@@ -57,7 +58,8 @@ constexpr int kTileN = 128;           // weight rows per tile (MMA M)
 constexpr int kTileK = 64;            // K per stage: one 128-byte swizzle row of fp16
 constexpr int kConvWarps = 8;         // two per TMEM lane quarter, alternating K steps
 constexpr int kEpiWarp0 = 2 + kConvWarps;
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;   // 14 warps
+constexpr int kEpiWarps = 8;          // two per TMEM lane quarter, alternating 32-token chunks
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;   // 18 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kPBytes = kTileN * kTileK / 4;   // 2 KB of codes per stage
 // at least this much dynamic shared memory, so that one CTA fits per SM and
@@ -98,7 +100,6 @@ struct GemmParams {
   const float* s_w;      // [1]
   float* Y;              // [M][N]
   int32_t* acc;          // [M][N] or null
-  int relu2;
   WsHeader* status;
 };
 
@@ -182,6 +183,29 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   }
 }
 
+// Warp-wide wait: lane 0 polls (with a short sleep between polls when
+// `sleepy`, for waits that are long by design), then every lane confirms the
+// completed phase once, which gives each of them the barrier's acquire
+// ordering. Returns the same verdict in every lane.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t deadline, volatile int* abort_flag,
+                                          bool sleepy) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  if (lane == 0) {
+    for (int n = 1;; ++n) {
+      if (mbar_try_wait(bar, parity)) break;
+      if (sleepy) __nanosleep(64);
+      if ((n & 15) == 0 && (*abort_flag || global_ns() > deadline)) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  if (ok) ok = mbar_wait_until(bar, parity, deadline);
+  return __all_sync(0xffffffffu, ok);
+}
+
 template <typename Ctl>
 __device__ __forceinline__ void raise_abort(Ctl* ctl, WsHeader* status, uint32_t where) {
   if (atomicExch(&ctl->abort, 1) == 0) report_status(status, BL_ERR_TIMEOUT, where);
@@ -200,7 +224,7 @@ __device__ __forceinline__ uint32_t pair_word(uint32_t w_lo, uint32_t w_hi) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <class C>
+template <class C, bool RELU2, bool ACC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                    const GemmParams p) {
@@ -231,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->accfull[b], 1);
-      mbar_init(&ctl->accempty[b], 4);
+      mbar_init(&ctl->accempty[b], kEpiWarps);
     }
     mbar_init(&ctl->done, 1);
     ctl->abort = 0;
@@ -377,8 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps kEpiWarp0 .. kEpiWarp0 + 3) ----------------
+    // ---------------- epilogue (warps kEpiWarp0 .. kEpiWarp0 + kEpiWarps - 1) ----------------
     const int quarter = warp & 3;
+    const int half = (warp - kEpiWarp0) >> 2;            // this warp's chunks: c % 2 == half
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sw = p.s_w[0];
     int local = 0;
@@ -386,32 +411,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tn = tile / tiles_m, tm = tile % tiles_m;
       const int b = C::kAccBufs == 2 ? (local & 1) : 0;
       const uint32_t use = static_cast<uint32_t>(C::kAccBufs == 2 ? (local >> 1) : local);
-      const bool got = wait_or_abort(&ctl->accfull[b], use & 1u, deadline, abort_flag);
-      if (!__all_sync(0xffffffffu, got)) {
+      if (!warp_wait(&ctl->accfull[b], use & 1u, deadline, abort_flag, true)) {
         if (lane == 0) raise_abort(ctl, p.status, 0x700u + blockIdx.x);
         break;
       }
       tc_fence_after();
       const int n = tn * kTileN + quarter * 32 + lane;
+      const bool n_ok = n < p.N;
 #pragma unroll 1
-      for (int c = 0; c < kTileM / 32; ++c) {
+      for (int c = half; c < kTileM / 32; c += 2) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + b * kTileM + c * 32, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         const int tok0 = tm * kTileM + c * 32;
         // lane j holds the dequant factor of token tok0 + j
         const float my_c = tok0 + lane < p.M ? dequant_factor(sw, p.m[tok0 + lane]) : 0.0f;
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (tok0 >= p.M) continue;
+        float* yp = p.Y + static_cast<size_t>(tok0) * p.N + n;
+        int32_t* ap = ACC ? p.acc + static_cast<size_t>(tok0) * p.N + n : nullptr;
+        const int jmax = min(32, p.M - tok0);
+        if (jmax == 32 && n_ok) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float cj = __shfl_sync(0xffffffffu, my_c, j);
-          const int tok = tok0 + j;
-          if (tok < p.M && n < p.N) {
+          for (int j = 0; j < 32; ++j) {
             const float accf = __uint_as_float(v[j]);
-            float y = __fmul_rn(accf, cj);
-            if (p.relu2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
-            const size_t o = static_cast<size_t>(tok) * p.N + n;
-            p.Y[o] = y;
-            if (p.acc != nullptr) p.acc[o] = __float2int_rn(accf);
+            float y = __fmul_rn(accf, __shfl_sync(0xffffffffu, my_c, j));
+            if constexpr (RELU2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
+            *yp = y;
+            yp += p.N;
+            if constexpr (ACC) {
+              *ap = __float2int_rn(accf);
+              ap += p.N;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float accf = __uint_as_float(v[j]);
+            float y = __fmul_rn(accf, __shfl_sync(0xffffffffu, my_c, j));
+            if constexpr (RELU2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
+            if (j < jmax && n_ok) {
+              *yp = y;
+              if constexpr (ACC) *ap = __float2int_rn(accf);
+            }
+            yp += p.N;
+            if constexpr (ACC) ap += p.N;
           }
         }
       }
@@ -487,12 +530,12 @@ cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStr
   p.s_w = g.s_w;
   p.Y = g.Y;
   p.acc = g.acc;
-  p.relu2 = g.relu2 ? 1 : 0;
   p.status = status;
   const int tiles = ((g.N + kTileN - 1) / kTileN) * ((g.M + C::kTileM - 1) / C::kTileM);
   const int grid = std::max(1, std::min(tiles, sm_count()));
   const size_t smem = C::smem_bytes();
-  auto kern = gemm_tc_kernel<C>;
+  auto kern = g.relu2 ? (g.acc != nullptr ? gemm_tc_kernel<C, true, true> : gemm_tc_kernel<C, true, false>)
+                      : (g.acc != nullptr ? gemm_tc_kernel<C, false, true> : gemm_tc_kernel<C, false, false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};

@@ -119,7 +119,7 @@ def test_forward_tiny_case():
     check_forward(W, X)
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 16, 17])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 16, 17])
 def test_forward_token_counts_ragged_rows(M):
     # N = 203 rows is ragged for every row-group size; K = 320 spans several 16-byte chunks per lane pass
     W = WL.gaussian_weights(203, 320, 0.02, seed=40 + M, outlier_frac=0.01)
@@ -279,7 +279,7 @@ def test_forward_long_k_and_tiny_n():
         check_forward(W, X)
 
 
-# ------------------------------------------------- tensor-core GEMM (M >= 17)
+# ------------------------------------------------- tensor-core GEMM (M >= 9)
 @pytest.mark.parametrize("M,K,N", [(17, 64, 128), (64, 320, 203), (128, 2560, 640), (129, 576, 130),
                                    (300, 2560, 257), (1000, 128, 384)])
 def test_gemm_path_ragged_tiles(M, K, N):
