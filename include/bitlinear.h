@@ -208,6 +208,9 @@ BL_API bl_status bitlinear_quant_act_tc(const void* X, int x_dtype, int M, int K
  * unpacked on chip and multiplied with 8-bit activations). Any M >= 0; the
  * result equals bitlinear_forward on the unquantized input.
  *   workspace >= 256 bytes (its status word; see bitlinear_workspace_status).
+ *             With 256 + 4 * M * N bytes, few tokens (M <= 128) may cut K into
+ *             parts run on more SMs, their exact integer partial sums added
+ *             in the workspace.
  */
 BL_API bl_status bitlinear_forward_tc(const void* act, const float* m, int M, int K,
                                const uint8_t* packed, const float* s_w, int N,

@@ -211,7 +211,8 @@ def forward_tc(act: torch.Tensor, m: torch.Tensor, packed: torch.Tensor, s_w: to
         raise ValueError(f"packed has {packed.shape[1]} bytes per row, expected K/4 = {K // 4}")
     Y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=act.device)
     acc = torch.empty((M, N), dtype=torch.int32, device=act.device) if return_acc else None
-    ws = _workspace(workspace, 256)
+    # room for [M][N] int32 partial sums lets few tokens cut K across more SMs
+    ws = _workspace(workspace, 256 + (4 * M * N if M <= 128 else 0))
     check(_lib.lib().bitlinear_forward_tc(_ptr(act), _ptr(m), M, K, _ptr(packed), _ptr(s_w), N, _ptr(Y), _ptr(acc),
                                           _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_forward_tc")
     return (Y, acc) if return_acc else Y

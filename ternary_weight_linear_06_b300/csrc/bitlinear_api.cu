@@ -43,23 +43,29 @@ bool valid_dtype(int d) { return d == BL_DTYPE_F32 || d == BL_DTYPE_BF16; }
 
 bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CUDA; }
 
-// Forward workspace: header | q (M*K fp16 or int8) | m [M] | qsum [M]
+// A GEMM with its K cut into parts needs an [M][N] int32 scratch for the
+// partial sums (the forward takes the GEMM from kGemmMinTokens tokens;
+// bitlinear_forward_tc for any count).
+bool uses_split(int M, int N, int K) { return gemm_splits(M, N, K) > 1; }
+
+// Forward workspace: header | q (M*K fp16 or int8) | m [M] | qsum [M] | split-K sums [M*N] int32
 // Batch workspace: header | q of every problem (M_p * K_p int8 each) | m of every problem
 struct FwdLayout {
-  size_t q, m, qsum, total;
+  size_t q, m, qsum, accw, total;
 };
-FwdLayout fwd_layout(int M, int K) {
+FwdLayout fwd_layout(int M, int N, int K) {
   FwdLayout L;
   L.q = sizeof(WsHeader);
   L.m = align_up(L.q + static_cast<size_t>(M) * K * 2, 256);
   L.qsum = align_up(L.m + 4 * static_cast<size_t>(M), 256);
-  L.total = align_up(L.qsum + 4 * static_cast<size_t>(M), 256);
+  L.accw = align_up(L.qsum + 4 * static_cast<size_t>(M), 256);
+  L.total = uses_split(M, N, K) ? align_up(L.accw + 4 * static_cast<size_t>(M) * N, 256) : L.accw;
   return L;
 }
 
-// FFN workspace: header | qx | mx | qsx | h [M*F] | hmax [M] | qh | mh | qsh
+// FFN workspace: header | qx | mx | qsx | h [M*F] | hmax [M] | qh | mh | qsh | split-K sums
 struct FfnLayout {
-  size_t qx, mx, qsx, h, hmax, qh, mh, qsh, total;
+  size_t qx, mx, qsx, h, hmax, qh, mh, qsh, accw, total;
 };
 FfnLayout ffn_layout(int M, int D, int F) {
   FfnLayout L;
@@ -72,7 +78,9 @@ FfnLayout ffn_layout(int M, int D, int F) {
   L.qh = align_up(L.hmax + m4, 256);
   L.mh = align_up(L.qh + static_cast<size_t>(M) * F * 2, 256);
   L.qsh = align_up(L.mh + m4, 256);
-  L.total = align_up(L.qsh + m4, 256);
+  L.accw = align_up(L.qsh + m4, 256);
+  const bool split = uses_split(M, F, D) || uses_split(M, D, F);
+  L.total = split ? align_up(L.accw + 4 * static_cast<size_t>(M) * std::max(D, F), 256) : L.accw;
   return L;
 }
 
@@ -95,7 +103,7 @@ GemvProblem make_problem(int M, int K, const uint8_t* packed, const float* s_w, 
 }
 
 GemmProblem make_gemm(int M, int K, const uint8_t* packed, const float* s_w, int N, const void* act, const float* m,
-                      float* Y, int32_t* acc, bool relu2) {
+                      float* Y, int32_t* acc, bool relu2, int32_t* acc_ws) {
   GemmProblem g = {};
   g.Wp = packed;
   g.s_w = s_w;
@@ -107,6 +115,7 @@ GemmProblem make_gemm(int M, int K, const uint8_t* packed, const float* s_w, int
   g.Y = Y;
   g.acc = acc;
   g.relu2 = relu2;
+  g.acc_ws = uses_split(M, N, K) ? acc_ws : nullptr;
   return g;
 }
 
@@ -152,7 +161,7 @@ size_t bitlinear_workspace_bytes(int op, int M, int N, int K) {
       return sizeof(WsHeader) + pack_scratch_bytes();
     case BL_OP_FORWARD:
       if (M < 0 || !valid_nk(N, K)) return 0;
-      return fwd_layout(M, K).total;
+      return fwd_layout(M, N, K).total;
     case BL_OP_FORWARD_BATCH:     // M = total tokens of the batch, K = the largest K
       if (M < 0 || (M > 0 && !valid_k(K))) return 0;
       return sizeof(WsHeader) + align_up(static_cast<size_t>(M) * (M > 0 ? K : 0), 256) +
@@ -199,14 +208,14 @@ bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K, const uint
   if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
     return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FwdLayout L = fwd_layout(M, K);
+  const FwdLayout L = fwd_layout(M, N, K);
   float* m = at<float>(workspace, L.m);
   if (M >= kGemmMinTokens) {
     // prefill: fp16 activations in the tensor-core order, then the tcgen05 GEMM
     void* act = at<void>(workspace, L.q);
     if (launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, nullptr, nullptr, true, st) != cudaSuccess)
       return BL_ERR_CUDA;
-    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false),
+    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false, at<int32_t>(workspace, L.accw)),
                                  static_cast<WsHeader*>(workspace), true, st));
   }
   int8_t* q = at<int8_t>(workspace, L.q);
@@ -284,9 +293,10 @@ bl_status bitlinear_forward_q8(const int8_t* q, const float* m, int M, int K, co
     return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (M >= kGemmMinTokens) {
-    void* act = at<void>(workspace, fwd_layout(M, K).q);
+    const FwdLayout L = fwd_layout(M, N, K);
+    void* act = at<void>(workspace, L.q);
     if (launch_widen_pair(q, M, K, act, true, st) != cudaSuccess) return BL_ERR_CUDA;
-    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false),
+    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false, at<int32_t>(workspace, L.accw)),
                                  static_cast<WsHeader*>(workspace), true, st));
   }
   GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
@@ -318,7 +328,11 @@ bl_status bitlinear_forward_tc(const void* act, const float* m, int M, int K, co
     return BL_ERR_ALIGN;
   if (workspace_bytes < sizeof(WsHeader)) return BL_ERR_WORKSPACE;
   if (bl_status s = check_device(); s != BL_OK) return s;
-  return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false),
+  // with room for the [M][N] partial sums right after the header, few tokens
+  // may cut K across more SMs
+  const size_t accw = sizeof(WsHeader);
+  int32_t* acc_ws = workspace_bytes >= accw + 4 * static_cast<size_t>(M) * N ? at<int32_t>(workspace, accw) : nullptr;
+  return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false, acc_ws),
                                static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
 }
 
@@ -344,11 +358,14 @@ bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t*
     float* mh = at<float>(workspace, L.mh);
     WsHeader* hdr = static_cast<WsHeader*>(workspace);
     if (launch_quant(X, x_dtype, M, D, eps, QLayout::kPairF16, ax, mx, nullptr, nullptr, true, st) != cudaSuccess ||
-        launch_gemm(make_gemm(M, D, up, s_up, F, ax, mx, h, nullptr, true), hdr, true, st) != cudaSuccess ||
+        launch_gemm(make_gemm(M, D, up, s_up, F, ax, mx, h, nullptr, true, at<int32_t>(workspace, L.accw)), hdr,
+                    true, st) != cudaSuccess ||
         launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kPairF16, ah, mh, nullptr, nullptr, true, st) !=
             cudaSuccess)
       return BL_ERR_CUDA;
-    return from_cuda(launch_gemm(make_gemm(M, F, down, s_down, D, ah, mh, Y, nullptr, false), hdr, true, st));
+    return from_cuda(launch_gemm(make_gemm(M, F, down, s_down, D, ah, mh, Y, nullptr, false,
+                                           at<int32_t>(workspace, L.accw)),
+                                 hdr, true, st));
   }
   int8_t* qx = at<int8_t>(workspace, L.qx);
   float* mx = at<float>(workspace, L.mx);

@@ -96,6 +96,8 @@ using CfgNarrow = Cfg<128, 8, 2>;   // 128 tokens (few tokens), two accumulators
 
 struct GemmParams {
   int M, N, K;
+  int splits;            // K is cut into this many parts, one work unit each
+  int32_t* acc_ws;       // splits > 1: [M][N] int32 partial-sum target (zeroed)
   const float* m;        // [M] per-token scales
   const float* s_w;      // [1]
   float* Y;              // [M][N]
@@ -224,7 +226,7 @@ __device__ __forceinline__ uint32_t pair_word(uint32_t w_lo, uint32_t w_hi) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <class C, bool RELU2, bool ACC>
+template <class C, bool RELU2, bool ACC, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                    const GemmParams p) {
@@ -246,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tiles_m = (p.M + kTileM - 1) / kTileM;
   const int tiles = tiles_n * tiles_m;
   const int ktiles = p.K / kTileK;
+  // work units: (tile, K part); a tile's parts are consecutive units, so they
+  // run on different CTAs at the same time
+  const int splits = SPLIT ? p.splits : 1;
+  const int units = tiles * splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -284,9 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int tile = u / splits, kp = u - tile * splits;
         const int tn = tile / tiles_m, tm = tile % tiles_m;
-        for (int kt = 0; kt < ktiles; ++kt) {
+        const int kb = kp * ktiles / splits, ke = (kp + 1) * ktiles / splits;
+        for (int kt = kb; kt < ke; ++kt) {
           if (!wait_or_abort(&ctl->empty[s], ph ^ 1u, deadline, abort_flag)) {
             raise_abort(ctl, p.status, 0x300u + blockIdx.x);
             ok = false;
@@ -315,7 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       int local = 0;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++local) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++local) {
+        const int kp = u % splits;
+        const int kb = kp * ktiles / splits, ke = (kp + 1) * ktiles / splits;
         const int b = C::kAccBufs == 2 ? (local & 1) : 0;
         const uint32_t use = static_cast<uint32_t>(C::kAccBufs == 2 ? (local >> 1) : local);
         if (!wait_or_abort(&ctl->accempty[b], (use & 1u) ^ 1u, deadline, abort_flag)) {
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + kAccCol + b * kTileM;
-        for (int kt = 0; kt < ktiles; ++kt) {
+        for (int kt = kb; kt < ke; ++kt) {
           if (!wait_or_abort(&ctl->aready[s], ph, deadline, abort_flag) ||
               !wait_or_abort(&ctl->full[s], ph, deadline, abort_flag)) {
             raise_abort(ctl, p.status, 0x500u + blockIdx.x);
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = sw128_desc(smem_u32(sB + s * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)
-            mma_f16_tmem_a<C::kIdesc>(d, a + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), (kt | kk) != 0 ? 1u : 0u);
+            mma_f16_tmem_a<C::kIdesc>(d, a + kk * 8, bdesc + static_cast<uint64_t>(kk * 2), (kt != kb || kk != 0) ? 1u : 0u);
           mma_commit(&ctl->empty[s]);
           if (++s == kStages) {
             s = 0;
@@ -359,8 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph = 0;
     bool ok = true;
     int step = 0;                                        // K steps of all tiles, in order
-    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-      for (int kt = 0; kt < ktiles; ++kt, ++step) {
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const int kp = u % splits;
+      const int kb = kp * ktiles / splits, ke = (kp + 1) * ktiles / splits;
+      for (int kt = kb; kt < ke; ++kt, ++step) {
         if ((step & 1) != parity) {
           if (++s == kStages) {
             s = 0;
@@ -407,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sw = p.s_w[0];
     int local = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++local) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+      const int tile = u / splits;
       const int tn = tile / tiles_m, tm = tile % tiles_m;
       const int b = C::kAccBufs == 2 ? (local & 1) : 0;
       const uint32_t use = static_cast<uint32_t>(C::kAccBufs == 2 ? (local >> 1) : local);
@@ -427,6 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float my_c = tok0 + lane < p.M ? dequant_factor(sw, p.m[tok0 + lane]) : 0.0f;
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (tok0 >= p.M) continue;
+        if constexpr (SPLIT) {
+          // exact integer partial sums, added in any order
+          int32_t* wp = p.acc_ws + static_cast<size_t>(tok0) * p.N + n;
+          const int jmax = min(32, p.M - tok0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j < jmax && n_ok) atomicAdd(wp, __float2int_rn(__uint_as_float(v[j])));
+            wp += p.N;
+          }
+          continue;
+        }
         float* yp = p.Y + static_cast<size_t>(tok0) * p.N + n;
         int32_t* ap = ACC ? p.acc + static_cast<size_t>(tok0) * p.N + n : nullptr;
         const int jmax = min(32, p.M - tok0);
@@ -471,6 +495,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
+// After a split-K GEMM: y = fp32(acc * fp32(fp32(s_w * m) / 127)) (then ReLU^2
+// for the FFN up projection) from the summed integer accumulators. One CTA
+// row per token (blockIdx.y), threads over the outputs.
+__global__ void __launch_bounds__(256) split_finalize_kernel(const int32_t* __restrict__ acc_ws, int M, int N,
+                                                             const float* __restrict__ m,
+                                                             const float* __restrict__ s_w, float* __restrict__ Y,
+                                                             int32_t* __restrict__ acc, int relu2) {
+  pdl_wait();
+  pdl_trigger();
+  const int tok = blockIdx.y;
+  const float c = dequant_factor(s_w[0], m[tok]);
+  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
+    const size_t o = static_cast<size_t>(tok) * N + n;
+    const int v = acc_ws[o];
+    float y = __fmul_rn(static_cast<float>(v), c);
+    if (relu2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
+    Y[o] = y;
+    if (acc != nullptr) acc[o] = v;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side: tensor maps (driver entry point looked up once) and the launch.
 // ---------------------------------------------------------------------------
@@ -510,7 +555,7 @@ int sm_count() {
 
 
 template <class C>
-cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st) {
+cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st, int splits) {
   CUtensorMap tm_act, tm_codes;
   // activations: fp16 [M][K] (pair order within 16-column groups)
   if (!make_map_2d(&tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.act, static_cast<uint64_t>(g.K),
@@ -526,16 +571,21 @@ cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStr
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
+  p.splits = std::max(1, splits);
+  p.acc_ws = g.acc_ws;
   p.m = g.m;
   p.s_w = g.s_w;
   p.Y = g.Y;
   p.acc = g.acc;
   p.status = status;
   const int tiles = ((g.N + kTileN - 1) / kTileN) * ((g.M + C::kTileM - 1) / C::kTileM);
-  const int grid = std::max(1, std::min(tiles, sm_count()));
+  const int grid = std::max(1, std::min(tiles * p.splits, sm_count()));
   const size_t smem = C::smem_bytes();
-  auto kern = g.relu2 ? (g.acc != nullptr ? gemm_tc_kernel<C, true, true> : gemm_tc_kernel<C, true, false>)
-                      : (g.acc != nullptr ? gemm_tc_kernel<C, false, true> : gemm_tc_kernel<C, false, false>);
+  auto kern = p.splits > 1 ? gemm_tc_kernel<C, false, false, true>
+               : g.relu2 ? (g.acc != nullptr ? gemm_tc_kernel<C, true, true, false>
+                                              : gemm_tc_kernel<C, true, false, false>)
+                         : (g.acc != nullptr ? gemm_tc_kernel<C, false, true, false>
+                                              : gemm_tc_kernel<C, false, false, false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -562,16 +612,45 @@ double tile_cost(int M, int N, int tile_m, bool single_acc, int sms) {
 
 }  // namespace
 
+int gemm_splits(int M, int N, int K) {
+  if (M < 1 || M > CfgNarrow::kTileM) return 1;
+  const int sms = sm_count();
+  const int tiles = (N + kTileN - 1) / kTileN;      // one 128-token tile column
+  const int ktiles = K / kTileK;
+  if (2 * tiles > sms || ktiles < 8) return 1;
+  // enough parts to fill the SMs, each of at least four K steps
+  return std::max(1, std::min(sms / tiles, ktiles / 4));
+}
+
 cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   const int sms = sm_count();
-  if (g.M <= CfgNarrow::kTileM) return launch_cfg<CfgNarrow>(g, status, pdl, st);
+  if (g.M <= CfgNarrow::kTileM) {
+    const int splits = gemm_splits(g.M, g.N, g.K);
+    if (splits > 1 && g.acc_ws != nullptr) {
+      cudaError_t err = cudaMemsetAsync(g.acc_ws, 0, static_cast<size_t>(g.M) * g.N * 4, st);
+      if (err == cudaSuccess) err = launch_cfg<CfgNarrow>(g, status, false, st, splits);
+      if (err != cudaSuccess) return err;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(std::min((g.N + 255) / 256, 64)), static_cast<unsigned>(g.M));
+      cfg.blockDim = dim3(256);
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, split_finalize_kernel, static_cast<const int32_t*>(g.acc_ws), g.M, g.N, g.m,
+                                g.s_w, g.Y, g.acc, g.relu2 ? 1 : 0);
+    }
+    return launch_cfg<CfgNarrow>(g, status, pdl, st, 1);
+  }
   const double wide = tile_cost(g.M, g.N, CfgWide::kTileM, true, sms);
   const double mid = tile_cost(g.M, g.N, CfgMid::kTileM, false, sms);
   const double narrow = tile_cost(g.M, g.N, CfgNarrow::kTileM, false, sms);
-  if (wide <= mid && wide <= narrow) return launch_cfg<CfgWide>(g, status, pdl, st);
-  if (mid <= narrow) return launch_cfg<CfgMid>(g, status, pdl, st);
-  return launch_cfg<CfgNarrow>(g, status, pdl, st);
+  if (wide <= mid && wide <= narrow) return launch_cfg<CfgWide>(g, status, pdl, st, 1);
+  if (mid <= narrow) return launch_cfg<CfgMid>(g, status, pdl, st, 1);
+  return launch_cfg<CfgNarrow>(g, status, pdl, st, 1);
 }
 
 }  // namespace bl

@@ -101,41 +101,41 @@ __device__ __forceinline__ uint4 to_quad(uint4 v) {
                     __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632));
 }
 
-// Copy tokens t0..t0+MT-1 of one problem into `sq` (layout above), with the
-// sum of their codes -> qs_out[t] and the dequant factor -> c_out[t]. All
-// threads take part.
-template <int MT>
-__device__ void stage_tokens(const DevProb& P, int t0, uint4* sq, float* c_out, int* qs_out, int (*s_ired)[MT]) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int K16 = P.K >> 4, C = P.K >> 6;
-#pragma unroll
-  for (int t = 0; t < MT; ++t) {
-    int qpart = 0;
-    const bool live = t0 + t < P.M;
-    const uint4* src = reinterpret_cast<const uint4*>(P.q + static_cast<size_t>(live ? t0 + t : 0) * P.K);
-    uint4* dst = sq + static_cast<size_t>(t) * K16;
-    for (int g = tid; g < K16; g += kThreads) {
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
-      if (live) {
-        const uint4 v = __ldg(src + g);
-        o = to_quad(v);
-        qpart = dp4a_su(static_cast<int>(v.x), 0x01010101u, qpart);
-        qpart = dp4a_su(static_cast<int>(v.y), 0x01010101u, qpart);
-        qpart = dp4a_su(static_cast<int>(v.z), 0x01010101u, qpart);
-        qpart = dp4a_su(static_cast<int>(v.w), 0x01010101u, qpart);
-      }
-      dst[(g & 3) * C + (g >> 2)] = o;
+// Copy the token rows of every span into shared memory in one pass: the
+// spans' rows lie end to end in the activation area (span j from uint4 offset
+// spans[j].act, MT rows of K/16 groups each), and thread tid takes the
+// 16-column groups tid, tid + kThreads, ... of that area, transposing each
+// into the order above. The sums of codes meet in shared memory by atomics;
+// then each token's dequant factor is computed once.
+template <int MT, int CAP>
+__device__ void stage_all(const BatchArgs<CAP>& a, Span<MT>* spans, int nspan, uint4* s_act, int* s_qs) {
+  const int tid = threadIdx.x;
+  const int total = spans[nspan - 1].act + MT * (a.prob[spans[nspan - 1].p].K >> 4);
+  int j = 0;
+  for (int g = tid; g < total; g += kThreads) {
+    while (j + 1 < nspan && spans[j + 1].act <= g) ++j;
+    const DevProb& P = a.prob[spans[j].p];
+    const int K16 = P.K >> 4, C = P.K >> 6;
+    const int local = g - spans[j].act;
+    const int t = local / K16, gg = local - t * K16;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (a.t0 + t < P.M) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(P.q + static_cast<size_t>(a.t0 + t) * P.K) + gg);
+      o = to_quad(v);
+      int qpart = dp4a_su(static_cast<int>(v.x), 0x01010101u, 0);
+      qpart = dp4a_su(static_cast<int>(v.y), 0x01010101u, qpart);
+      qpart = dp4a_su(static_cast<int>(v.z), 0x01010101u, qpart);
+      qpart = dp4a_su(static_cast<int>(v.w), 0x01010101u, qpart);
+      atomicAdd(&s_qs[j * MT + t], qpart);
     }
-    qpart = warp_sum(qpart);
-    if (lane == 0) s_ired[warp][t] = qpart;
+    s_act[spans[j].act + t * K16 + (gg & 3) * C + (gg >> 2)] = o;
   }
   __syncthreads();
-  if (tid < MT) {
-    int v = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) v += s_ired[w][tid];
-    qs_out[tid] = v;
-    c_out[tid] = t0 + tid < P.M ? dequant_factor(P.s_w[0], P.m_in[t0 + tid]) : 0.0f;
+  if (tid < nspan * MT) {
+    const int jj = tid / MT, t = tid - jj * MT;
+    const DevProb& P = a.prob[spans[jj].p];
+    spans[jj].qs[t] = s_qs[tid];
+    spans[jj].c[t] = a.t0 + t < P.M ? dequant_factor(P.s_w[0], P.m_in[a.t0 + t]) : 0.0f;
   }
   __syncthreads();
 }
@@ -151,7 +151,9 @@ __device__ __forceinline__ void run_span(const DevProb& P, const Span<MT>& S, co
   const int lane = threadIdx.x & 31;
   const int grp = lane / LPR, sub = lane % LPR;
   const int C = P.K >> 6;
-  const int nb = (C + LPR * U - 1) / (LPR * U);
+  const int n_per = (C + LPR - 1) / LPR;               // chunks per lane per row
+  const int nb = (n_per + U - 1) / U;                  // batches per row
+  const int Ue = (n_per + nb - 1) / nb;                // chunks per lane per batch, evenly split
   const int r0 = S.r0, r1 = S.r1;
   const int n_items = (r1 - r0 + G - 1) / G;
   const size_t rb = static_cast<size_t>(P.K) >> 2;
@@ -165,16 +167,16 @@ __device__ __forceinline__ void run_span(const DevProb& P, const Span<MT>& S, co
 #pragma unroll
       for (int i = 0; i < NA; ++i) acc[t][i] = 0;
     for (int b = 0; b < nb; ++b) {
-      const int c0 = b * (LPR * U) + sub;
-      const int lim = C - c0;
+      const int c0 = b * (LPR * Ue) + sub;
+      const int lim = C - c0;                 // chunk u exists when u < Ue and u * LPR < lim
       uint4 w[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        w[u] = (valid && u * LPR < lim) ? __ldg(wrow + c0 + u * LPR) : make_uint4(0u, 0u, 0u, 0u);
+        w[u] = (valid && u < Ue && u * LPR < lim) ? __ldg(wrow + c0 + u * LPR) : make_uint4(0u, 0u, 0u, 0u);
       const uint4* a0 = act + c0;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (u * LPR >= lim) break;
+        if (u >= Ue || u * LPR >= lim) break;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t wv = j == 0 ? w[u].x : j == 1 ? w[u].y : j == 2 ? w[u].z : w[u].w;
@@ -228,9 +230,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   extern __shared__ __align__(128) uint4 s_act[];
   __shared__ Span<MT> s_span[kMaxSpan];
   __shared__ int s_nspan;
-  __shared__ int s_ired[kWarps][MT];
+  __shared__ int s_qs[kMaxSpan * MT];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int r_begin = a.cta_row[blockIdx.x], r_end = a.cta_row[blockIdx.x + 1];
+  if (tid < kMaxSpan * MT) s_qs[tid] = 0;
   if (tid == 0) {
     int nspan = 0, items = 0, act = 0;
     if (r_begin < r_end) {
@@ -259,8 +262,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   pdl_wait();
   const int nspan = s_nspan;
   if (nspan == 0) return;
-  for (int j = 0; j < nspan; ++j)
-    stage_tokens<MT>(a.prob[s_span[j].p], a.t0, s_act + s_span[j].act, s_span[j].c, s_span[j].qs, s_ired);
+  stage_all<MT, CAP>(a, s_span, nspan, s_act, s_qs);
   // items are dealt round-robin over the warps across all spans (item i of
   // the CTA goes to warp i % kWarps); the rows of a span are contiguous in
   // HBM, so the CTA streams one region at a time
@@ -278,20 +280,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   }
 }
 
-// Lanes per row for a row of C 16-byte chunks: the choice that wastes the
-// fewest lane-chunk slots, more lanes on ties (and at least 4, so that one
-// lane per token can write the result).
+// Lanes per row for a row of C 16-byte chunks, from a cost model measured on
+// B300: a warp's item (32/LPR rows) costs about its chunks per lane plus one
+// (the reduction and the stores), so the cost per row is
+// (ceil(C/LPR) + 1) * LPR / 32. At least 4 lanes, so that one lane per token
+// can write the result; ties go to fewer lanes.
+int row_cost_x32(int C, int lpr) { return ((C + lpr - 1) / lpr + 1) * lpr; }
+
 int lpr_for_chunks(int C) {
   int best = 4;
-  long long best_num = -1, best_den = 1;
-  for (int lpr = 4; lpr <= 32; lpr *= 2) {
-    const long long den = static_cast<long long>(lpr) * ((C + lpr - 1) / lpr);
-    if (static_cast<long long>(C) * best_den >= best_num * den) {
-      best_num = C;
-      best_den = den;
-      best = lpr;
-    }
-  }
+  for (int lpr = 8; lpr <= 32; lpr *= 2)
+    if (row_cost_x32(C, lpr) < row_cost_x32(C, best)) best = lpr;
   return best;
 }
 
@@ -315,7 +314,7 @@ DevInfo dev_info() {
   return cached;
 }
 
-// Host-side plan for one launch: CTA runs balanced by bytes and the shared
+// Host-side plan for one launch: CTA runs balanced by the row cost model and the shared
 // memory the staged activations need. Returns 0 when the problems cannot
 // share one launch, else the dynamic shared-memory size.
 template <int CAP>
@@ -327,7 +326,7 @@ size_t plan(BatchArgs<CAP>& a, int mt, int sms, int* grid_out) {
     P.row_begin = rows;
     P.lpr = lpr_for_chunks(P.K >> 6);
     rows += P.N;
-    total += static_cast<long long>(P.N) * (P.K / 4);
+    total += static_cast<long long>(P.N) * row_cost_x32(P.K >> 6, P.lpr);
   }
   if (rows == 0) return 0;
   const int grid = std::max(1, std::min(std::min(kCtasPerSm * sms, kMaxCtas), rows));
@@ -337,7 +336,7 @@ size_t plan(BatchArgs<CAP>& a, int mt, int sms, int* grid_out) {
   a.cta_row[0] = 0;
   for (int r = 0; r < rows && c < grid; ++r) {
     while (a.prob[p].row_begin + a.prob[p].N <= r) ++p;
-    cum += a.prob[p].K / 4;
+    cum += row_cost_x32(a.prob[p].K >> 6, a.prob[p].lpr);
     while (c < grid && cum * grid >= total * c) a.cta_row[c++] = r + 1;
   }
   while (c <= grid) a.cta_row[c++] = rows;

@@ -70,7 +70,11 @@ struct GemmProblem {
   float* Y;              // [M][N]
   int32_t* acc;          // [M][N] or null
   bool relu2;            // FFN up: write h = relu(y)^2
+  int32_t* acc_ws;       // [M][N] int32 scratch for a split-K run, or null (no split)
 };
+// How many K parts a GEMM of these sizes is cut into (1: no split). Split runs
+// need an [M][N] int32 scratch (GemmProblem::acc_ws).
+int gemm_splits(int M, int N, int K);
 // Tokens from which the forward takes the tensor-core GEMM instead of the GEMV
 // (measured on B300: the GEMV is faster up to 8 tokens on the 2B-class shapes,
 // the GEMM from 12).

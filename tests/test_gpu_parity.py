@@ -414,3 +414,29 @@ def test_gemm_full_size_prefill_sampled_rows(shape):
 def test_gemm_70b_class_shape_sampled_rows(M):
     K, N = 8192, 8192
     _check_sampled(WL.gaussian_weights(N, K, 0.01, seed=M, outlier_frac=0.001), WL.student_t(M, K, seed=M + 1), 19)
+
+
+def test_gemm_split_k_ffn_few_tokens():
+    # 16 tokens: the GEMM cuts K into parts (exact integer partial sums added
+    # in the workspace), then ReLU^2 and the requantization run on the sums
+    D, F, M = 2560, 6912, 16
+    Wu = WL.decode_weights("up", 5)
+    Wd = WL.decode_weights("down", 5)
+    X = WL.student_t(M, D, seed=96)
+    up, s_up = BL.pack(dev(Wu))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sd, td = O.pack_weights(Wd)
+    Y = BL.ffn(dev(X), up, s_up, down, s_down)
+    Y_ref, _ = O.ffn(X, tu, su, td, sd)
+    assert_y(host(Y), Y_ref)
+    assert BL.workspace_status() == 0
+
+
+@pytest.mark.parametrize("M", [9, 12, 33, 128])
+def test_gemm_split_k_token_counts(M):
+    for shape in ("qo", "kv", "down"):
+        K, N = WL.SHAPES_2B[shape]
+        W = WL.decode_weights(shape, 8)
+        xb = WL.batched_activations_bf16(M, K, seed=800 + M)
+        check_forward(W, xb, x_is_bf16_bits=True)
