@@ -120,20 +120,28 @@ class ClockSampler:
 
 # --------------------------------------------------------- decode workload
 def build_decode(torch, BL, WL, layers: int, device):
-    """Packs the 30x4 weight matrices and draws the 120 activation rows."""
+    """Packs the 30x4 weight matrices and draws the 120 activation rows. The
+    inputs of all problems live end to end in one device buffer and the
+    outputs in another (each row 16-byte aligned), as a caller of the batched
+    call keeps them, so one copy moves all inputs and one all outputs."""
+    specs = [(layer, shape) + WL.SHAPES_2B[shape] for layer in range(layers) for shape in SHAPE_ORDER]
+    x_flat = torch.empty(sum(K for _, _, K, _ in specs), dtype=torch.float32, device=device)
+    y_flat = torch.empty(sum(N for _, _, _, N in specs), dtype=torch.float32, device=device)
     mats = []
-    for layer in range(layers):
-        for shape in SHAPE_ORDER:
-            K, N = WL.SHAPES_2B[shape]
-            W = torch.from_numpy(WL.decode_weights(shape, layer)).to(device)
-            packed, s_w = BL.pack(W)
-            del W
-            X = torch.from_numpy(WL.decode_activations(shape, layer)).to(device)
-            Y = torch.empty((1, N), dtype=torch.float32, device=device)
-            mats.append({"shape": shape, "layer": layer, "K": K, "N": N, "packed": packed, "s_w": s_w, "X": X,
-                         "Y": Y})
+    xo = yo = 0
+    for layer, shape, K, N in specs:
+        W = torch.from_numpy(WL.decode_weights(shape, layer)).to(device)
+        packed, s_w = BL.pack(W)
+        del W
+        X = x_flat[xo:xo + K].view(1, K)
+        X.copy_(torch.from_numpy(WL.decode_activations(shape, layer)))
+        Y = y_flat[yo:yo + N].view(1, N)
+        xo += K
+        yo += N
+        mats.append({"shape": shape, "layer": layer, "K": K, "N": N, "packed": packed, "s_w": s_w, "X": X,
+                     "Y": Y})
     torch.cuda.synchronize()
-    return mats
+    return mats, x_flat, y_flat
 
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
@@ -189,7 +197,7 @@ def run_ours(args):
     device = torch.device("cuda", local_rank)
     peaks, peak_src = measured_peaks()
 
-    mats = build_decode(torch, BL, WL, args.layers, device)
+    mats, x_flat, y_flat = build_decode(torch, BL, WL, args.layers, device)
     ws = BL.Workspace(1 << 16, device)
     stream = torch.cuda.Stream(device)
     bytes_step = packed_bytes(mats)
@@ -281,29 +289,24 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         chained_s = time_graph(torch, gc, chained_steps, 3, stream)
 
-    # end-to-end: pinned host X -> device, the batched call, device Y -> pinned host
-    xs_host = [torch.empty_like(m["X"], device="cpu").pin_memory() for m in mats]
-    for h, m in zip(xs_host, mats):
-        h.copy_(m["X"].cpu())
-    ys_host = [torch.empty_like(m["Y"], device="cpu").pin_memory() for m in mats]
-    h2d = sum(x.numel() * 4 for x in xs_host)
-    d2h = sum(y.numel() * 4 for y in ys_host)
+    # end-to-end: pinned host X -> device (one copy of the 120 input rows), the
+    # batched call, device Y -> pinned host (one copy of the 120 output rows)
+    x_host = x_flat.cpu().pin_memory()
+    y_host = torch.empty_like(y_flat, device="cpu").pin_memory()
+    h2d = x_host.numel() * 4
+    d2h = y_host.numel() * 4
     e_steps = max(1, min(args.steps, 200))
     with torch.cuda.stream(stream):
         for _ in range(2):
-            for h, m in zip(xs_host, mats):
-                m["X"].copy_(h, non_blocking=True)
+            x_flat.copy_(x_host, non_blocking=True)
             g.replay()
-            for h, m in zip(ys_host, mats):
-                h.copy_(m["Y"], non_blocking=True)
+            y_host.copy_(y_flat, non_blocking=True)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e_steps):
-            for h, m in zip(xs_host, mats):
-                m["X"].copy_(h, non_blocking=True)
+            x_flat.copy_(x_host, non_blocking=True)
             g.replay()
-            for h, m in zip(ys_host, mats):
-                h.copy_(m["Y"], non_blocking=True)
+            y_host.copy_(y_flat, non_blocking=True)
         stream.synchronize()
         e2e_s = time.perf_counter() - t0
     e2e_value = bytes_step * e_steps / e2e_s / 1e9 * world
@@ -336,7 +339,8 @@ def run_ours(args):
                     "how": "the same 120 forwards as dependent bitlinear_forward calls in stream order "
                            "(programmatic dependent launch), CUDA graph"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "pinned host X -> device, graph replay, device Y -> pinned host, every step"},
+                "how": "pinned host -> device copy of the 120 input rows (one buffer), graph replay, device -> "
+                       "pinned host copy of the 120 output rows (one buffer), every step"},
         "gpu_launches": 2 * args.steps,
         "prefill": prefill,
         "clocks": clk,
@@ -542,6 +546,46 @@ def run_crossover(args):
     print(json.dumps(out))
 
 
+def run_large(args):
+    """70B-class shapes (hidden 8192, FFN 28672), swept over token counts: each
+    forward (quantization + GEMV or GEMM) timed alone with L2 flushed between
+    calls; GB/s of packed weights and integer TOPS (2*M*N*K)."""
+    import torch
+
+    import ternary_weight_linear_06_b300 as BL
+    from ternary_weight_linear_06_b300 import workloads as WL
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    ws = BL.Workspace(0, device)
+    peaks, _ = measured_peaks()
+    Ms = [1, 8, 64, 512, 2048]
+    out = {"what": "70B-class shapes: forward per token count (L2 flushed)", "M": Ms, "shapes": {}}
+    with torch.cuda.stream(stream):
+        for shape in ("attn", "up", "down"):
+            K, N = WL.SHAPES_70B[shape]
+            W = torch.from_numpy(WL.large_weights(shape)).to(device)
+            packed, s_w = BL.pack(W)
+            del W
+            rows = {"K": K, "N": N, "us": [], "GBps": [], "TOPS": []}
+            for M in Ms:
+                X = torch.from_numpy(WL.student_t(M, K, seed=40 + M)).to(device)
+                Y = torch.empty((M, N), dtype=torch.float32, device=device)
+                BL.forward(X, packed, s_w, out=Y, workspace=ws)
+                torch.cuda.synchronize()
+                t = time_each(torch, lambda: BL.forward(X, packed, s_w, out=Y, workspace=ws), args.prefill_iters,
+                              stream, flush)
+                rows["us"].append(round(t * 1e6, 2))
+                rows["GBps"].append(round(N * K / 4 / t / 1e9, 1))
+                rows["TOPS"].append(round(2.0 * M * N * K / t / 1e12, 1))
+                del X, Y
+            out["shapes"][shape] = rows
+    out["hbm_peak_gbs"] = peaks["hbm_gbs"]
+    out["tensor_peak_tflops"] = peaks["bf16_tflops"]
+    print(json.dumps(out))
+
+
 def run_prefill_only(args):
     import torch
 
@@ -572,6 +616,8 @@ def main():
     ap.add_argument("--prefill-iters", type=int, default=20)
     ap.add_argument("--prefill-shapes", default="", help="comma-separated subset of qo,kv,up,down")
     ap.add_argument("--prefill-no-ffn", action="store_true")
+    ap.add_argument("--large", action="store_true",
+                    help="70B-class shapes over token counts (prints its own JSON; not the bench line)")
     ap.add_argument("--crossover", action="store_true",
                     help="batched decode GEMV vs GEMM sweep (prints its own JSON; not the bench line)")
     args = ap.parse_args()
@@ -583,6 +629,8 @@ def main():
         run_prefill_only(args)
     elif args.crossover:
         run_crossover(args)
+    elif args.large:
+        run_large(args)
     else:
         run_ours(args)
 

@@ -335,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + kAccCol + b * kTileM;
         for (int kt = kb; kt < ke; ++kt) {
-          if (!wait_or_abort(&ctl->aready[s], ph, deadline, abort_flag) ||
-              !wait_or_abort(&ctl->full[s], ph, deadline, abort_flag)) {
+          // the converters waited for the stage's TMA bytes before they
+          // arrived on aready, so this one wait orders both operands
+          if (!wait_or_abort(&ctl->aready[s], ph, deadline, abort_flag)) {
             raise_abort(ctl, p.status, 0x500u + blockIdx.x);
             ok = false;
             break;

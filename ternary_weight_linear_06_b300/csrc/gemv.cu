@@ -330,6 +330,23 @@ size_t plan(BatchArgs<CAP>& a, int mt, int sms, int* grid_out) {
   }
   if (rows == 0) return 0;
   const int grid = std::max(1, std::min(std::min(kCtasPerSm * sms, kMaxCtas), rows));
+  // few long rows (one large matrix): widen the lane groups until every warp
+  // has items (rows / (32 / LPR)) to stream, at least two on average
+  for (;;) {
+    long long items = 0;
+    for (int i = 0; i < a.count; ++i) items += (a.prob[i].N + 32 / a.prob[i].lpr - 1) / (32 / a.prob[i].lpr);
+    if (items >= 2ll * grid * kWarps) break;
+    bool widened = false;
+    for (int i = 0; i < a.count; ++i)
+      if (a.prob[i].lpr < 32) {
+        a.prob[i].lpr *= 2;
+        widened = true;
+      }
+    if (!widened) break;
+  }
+  total = 0;
+  for (int i = 0; i < a.count; ++i)
+    total += static_cast<long long>(a.prob[i].N) * row_cost_x32(a.prob[i].K >> 6, a.prob[i].lpr);
   // boundaries: first row whose cumulative byte count reaches c/grid of the total
   int c = 1, p = 0;
   long long cum = 0;

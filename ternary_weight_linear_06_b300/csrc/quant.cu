@@ -138,7 +138,6 @@ template <int DT, int LAYOUT>
 cudaError_t launch_t(const void* X, int M, int K, float eps, void* q, float* m_out, int32_t* qsum_out,
                      const float* absmax_in, bool pdl, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(M));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -146,6 +145,7 @@ cudaError_t launch_t(const void* X, int M, int K, float eps, void* q, float* m_o
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(M));
   return cudaLaunchKernelEx(&cfg, quant_kernel<DT, LAYOUT>, X, K, eps, q, m_out, qsum_out, absmax_in);
 }
 

@@ -100,6 +100,22 @@ def test_quant_act_f32_and_bf16():
     np.testing.assert_array_equal(host(m), m_ref)
 
 
+def test_quant_act_many_rows_one_warp_per_row():
+    # 300 rows take the one-warp-per-row kernel; bf16 and fp32, both layouts
+    xb = WL.batched_activations_bf16(300, 2560, seed=33)
+    Xb = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    q_ref, m_ref = O.quant_act(O.bf16_bits_to_f32(xb))
+    q, m = BL.quant_act(Xb)
+    np.testing.assert_array_equal(host(q), q_ref)
+    np.testing.assert_array_equal(host(m).view(np.uint32), m_ref.view(np.uint32))
+    X = WL.prefill_activations(300, 6912, seed=34)
+    q_ref, m_ref = O.quant_act(X)
+    act, m = BL.quant_act_tc(dev(X))
+    np.testing.assert_array_equal(host(act).astype(np.int32).reshape(300, 6912 // 16, 8, 2).transpose(0, 1, 3, 2)
+                                  .reshape(300, 6912), q_ref)
+    np.testing.assert_array_equal(host(m).view(np.uint32), m_ref.view(np.uint32))
+
+
 # ----------------------------------------------------------------- forward
 def check_forward(W, X, x_is_bf16_bits=False):
     packed, s_w, t_ref, s_ref = check_pack(W)
@@ -388,7 +404,7 @@ def _sampled_rows(M, seed):
     rows = {0, 1, M - 1, M - 2, M // 2}
     for tile in (128, 192, 256):
         rows.update(r for r in (tile - 1, tile, 3 * tile - 1, 3 * tile) if r < M)
-    rows.update(rng.choice(M, size=24, replace=False).tolist())
+    rows.update(rng.choice(M, size=min(24, M), replace=False).tolist())
     return np.array(sorted(rows))
 
 
@@ -440,3 +456,11 @@ def test_gemm_split_k_token_counts(M):
         W = WL.decode_weights(shape, 8)
         xb = WL.batched_activations_bf16(M, K, seed=800 + M)
         check_forward(W, xb, x_is_bf16_bits=True)
+
+
+@pytest.mark.parametrize("shape,M", [("up", 64), ("down", 512), ("down", 9)])
+def test_large_ffn_shapes_sampled_rows(shape, M):
+    # 70B-class FFN shapes (K or N = 28672): the GEMM with split-K (64 and 9
+    # tokens) and with 128/192/256-token tiles (512 tokens)
+    K, N = WL.SHAPES_70B[shape]
+    _check_sampled(WL.large_weights(shape), WL.student_t(M, K, seed=M + K), 23)
