@@ -85,8 +85,9 @@ typedef enum {
   BL_OP_PACK = 0,          /* bitlinear_pack(N, K)                          */
   BL_OP_FORWARD = 1,       /* bitlinear_forward(M, N, K)                    */
   BL_OP_FFN = 2,           /* bitlinear_ffn(M, N = F (hidden), K = D (model)) */
-  BL_OP_FORWARD_BATCH = 3  /* bitlinear_forward_batch(M = total tokens of all
+  BL_OP_FORWARD_BATCH = 3, /* bitlinear_forward_batch(M = total tokens of all
                               problems, K = their largest K, N ignored)      */
+  BL_OP_FFN_GATED = 4      /* bitlinear_ffn_gated(M, N = F (hidden), K = D)  */
 } bl_op;
 
 /* Version of this ABI (major * 100 + minor). */
@@ -259,6 +260,20 @@ BL_API bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D,
                         const uint8_t* up, const float* s_up,
                         const uint8_t* down, const float* s_down, int F, float eps,
                         float* Y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Gated FFN block: Y = BitLinear_down(ReLU^2(BitLinear_gate(X)) * BitLinear_up(X)),
+ *   the squared ReLU of the report's section 2 (架构) in place of SwiGLU's SiLU
+ *   in a gated unit; gate and up quantize the same input once; the product h
+ *   = fp32(fp32(ReLU(y_gate)^2) * y_up) is requantized per token before down.
+ *   up, gate [F, D/4] uint8 + s_up, s_gate [1]; other arguments as bitlinear_ffn.
+ *   workspace >= bitlinear_workspace_bytes(BL_OP_FFN_GATED, M, F, D) bytes.
+ */
+BL_API bl_status bitlinear_ffn_gated(const void* X, int x_dtype, int M, int D,
+                              const uint8_t* up, const float* s_up,
+                              const uint8_t* gate, const float* s_gate,
+                              const uint8_t* down, const float* s_down, int F, float eps,
+                              float* Y, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Decode packed codes back to ternary values (the inverse of the packing of

@@ -39,6 +39,7 @@ Readings where the pages are silent (each repeated in the design notes):
   * storage code of a ternary value t is t + 1 in {0, 1, 2}; byte b of a row
     holds k = 4b + j in bits [2j, 2j+1] (little end first).
   * FFN: ungated up -> ReLU^2 -> requant (same eps) -> down; no norm between.
+  * gated FFN: h = fp32(fp32(ReLU(gate)^2) * up), then requant and down.
 """
 from __future__ import annotations
 
@@ -55,7 +56,7 @@ __all__ = [
     "round_rational_to_f32", "abs_sum_exact", "absmean_gamma", "weight_scale",
     "ternarize", "pack_codes", "unpack_codes", "pack_weights",
     "bf16_bits_to_f32", "quant_act", "int_matmul", "dequant", "forward",
-    "forward_packed", "relu2", "ffn", "tie_count",
+    "forward_packed", "relu2", "ffn", "ffn_gated", "tie_count",
 ]
 
 
@@ -250,4 +251,14 @@ def ffn(X, t_up, s_up, t_down, s_down, eps=EPS):
     """Ungated FFN block: up -> ReLU^2 -> requant -> down. Returns (Y, h)."""
     y_up = forward(X, t_up, s_up, eps)[0]
     h = relu2(y_up)
+    return forward(h, t_down, s_down, eps)[0], h
+
+
+def ffn_gated(X, t_up, s_up, t_gate, s_gate, t_down, s_down, eps=EPS):
+    """Gated FFN block (squared ReLU in place of SwiGLU's SiLU, [P1 §2]):
+    h = fp32(ReLU^2(gate(X)) * up(X)), requantized per token, then down.
+    gate and up are BitLinears on the same input. Returns (Y, h)."""
+    y_up = forward(X, t_up, s_up, eps)[0]
+    y_gate = forward(X, t_gate, s_gate, eps)[0]
+    h = (relu2(y_gate) * y_up).astype(np.float32)
     return forward(h, t_down, s_down, eps)[0], h

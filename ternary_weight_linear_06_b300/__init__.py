@@ -14,13 +14,14 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_DTYPE_I8, BL_MAX_BATCH, BL_OP_FFN, BL_OP_FORWARD,  # noqa: F401
+from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_DTYPE_I8, BL_MAX_BATCH, BL_OP_FFN, BL_OP_FFN_GATED,  # noqa: F401
+                   BL_OP_FORWARD,
                    BL_OP_FORWARD_BATCH, BL_OP_PACK, BitLinearError, ForwardDesc, check)
 
 EPS = 1e-5
 
 __all__ = ["pack", "quant_act", "quant_act_tc", "forward", "forward_batch", "forward_q8", "forward_tc",
-           "forward_noalloc", "ffn", "unpack", "workspace_bytes", "workspace_status",
+           "forward_noalloc", "ffn", "ffn_gated", "unpack", "workspace_bytes", "workspace_status",
            "Workspace", "BitLinearError", "EPS", "library_path"]
 
 
@@ -253,6 +254,27 @@ def ffn(X: torch.Tensor, up: torch.Tensor, s_up: torch.Tensor, down: torch.Tenso
     ws = _workspace(workspace, nb)
     check(_lib.lib().bitlinear_ffn(_ptr(X), _x_dtype(X), M, D, _ptr(up), _ptr(s_up), _ptr(down), _ptr(s_down), F,
                                    eps, _ptr(Y), _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_ffn")
+    return Y
+
+
+def ffn_gated(X: torch.Tensor, up: torch.Tensor, s_up: torch.Tensor, gate: torch.Tensor, s_gate: torch.Tensor,
+              down: torch.Tensor, s_down: torch.Tensor, eps: float = EPS, out: torch.Tensor | None = None,
+              workspace: Workspace | None = None, stream=None):
+    """Gated FFN: down(ReLU^2(gate(X)) * up(X)), each projection a BitLinear."""
+    _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+    for t, n in ((up, "up"), (gate, "gate"), (down, "down")):
+        _need_cuda(t, n, (torch.uint8,))
+    M, D = X.shape
+    F = up.shape[0]
+    if (up.shape[1] * 4 != D or tuple(gate.shape) != tuple(up.shape) or down.shape[0] != D
+            or down.shape[1] * 4 != F):
+        raise ValueError("gated FFN weight shapes do not match X")
+    Y = out if out is not None else torch.empty((M, D), dtype=torch.float32, device=X.device)
+    nb = workspace_bytes(BL_OP_FFN_GATED, M, F, D)
+    ws = _workspace(workspace, nb)
+    check(_lib.lib().bitlinear_ffn_gated(_ptr(X), _x_dtype(X), M, D, _ptr(up), _ptr(s_up), _ptr(gate), _ptr(s_gate),
+                                         _ptr(down), _ptr(s_down), F, eps, _ptr(Y), _ptr(ws), ws.numel(),
+                                         _stream(stream)), "bitlinear_ffn_gated")
     return Y
 
 

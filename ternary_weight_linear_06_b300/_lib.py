@@ -29,6 +29,7 @@ BL_OP_PACK = 0
 BL_OP_FORWARD = 1
 BL_OP_FFN = 2
 BL_OP_FORWARD_BATCH = 3
+BL_OP_FFN_GATED = 4
 BL_MAX_BATCH = 128
 
 
@@ -54,6 +55,7 @@ SIGNATURES = {
     "bitlinear_forward_tc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
     "bitlinear_forward_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp]),
     "bitlinear_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),
+    "bitlinear_ffn_gated": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "bitlinear_unpack": (_i, [_vp, _i, _i, _vp, _vp]),
     "bitlinear_workspace_status": (_i, [_vp, _vp]),
 }

@@ -64,10 +64,11 @@ FwdLayout fwd_layout(int M, int N, int K) {
 }
 
 // FFN workspace: header | qx | mx | qsx | h [M*F] | hmax [M] | qh | mh | qsh | split-K sums
+// (gated: then ReLU^2(gate) [M*F] after the split-K sums)
 struct FfnLayout {
-  size_t qx, mx, qsx, h, hmax, qh, mh, qsh, accw, total;
+  size_t qx, mx, qsx, h, hmax, qh, mh, qsh, accw, g, total;
 };
-FfnLayout ffn_layout(int M, int D, int F) {
+FfnLayout ffn_layout(int M, int D, int F, bool gated = false) {
   FfnLayout L;
   const size_t m4 = 4 * static_cast<size_t>(M);
   L.qx = sizeof(WsHeader);
@@ -80,7 +81,8 @@ FfnLayout ffn_layout(int M, int D, int F) {
   L.qsh = align_up(L.mh + m4, 256);
   L.accw = align_up(L.qsh + m4, 256);
   const bool split = uses_split(M, F, D) || uses_split(M, D, F);
-  L.total = split ? align_up(L.accw + 4 * static_cast<size_t>(M) * std::max(D, F), 256) : L.accw;
+  L.g = split ? align_up(L.accw + 4 * static_cast<size_t>(M) * std::max(D, F), 256) : L.accw;
+  L.total = gated ? align_up(L.g + 4 * static_cast<size_t>(M) * F, 256) : L.g;
   return L;
 }
 
@@ -167,8 +169,9 @@ size_t bitlinear_workspace_bytes(int op, int M, int N, int K) {
       return sizeof(WsHeader) + align_up(static_cast<size_t>(M) * (M > 0 ? K : 0), 256) +
              align_up(4 * static_cast<size_t>(M), 256);
     case BL_OP_FFN:
+    case BL_OP_FFN_GATED:
       if (M < 0 || !valid_nk(N, K) || !valid_k(N) || N == 0) return 0;
-      return ffn_layout(M, K, N).total;
+      return ffn_layout(M, K, N, op == BL_OP_FFN_GATED).total;
     default: return 0;
   }
 }
@@ -336,56 +339,100 @@ bl_status bitlinear_forward_tc(const void* act, const float* m, int M, int K, co
                                static_cast<WsHeader*>(workspace), true, static_cast<cudaStream_t>(stream)));
 }
 
-bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
-                        const uint8_t* down, const float* s_down, int F, float eps, float* Y, void* workspace,
-                        size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The FFN block: up (and gate) on one quantization of X, ReLU^2 (times the up
+// projection when gated), requantization, down. gate == nullptr: ungated.
+bl_status run_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
+                  const uint8_t* gate, const float* s_gate, const uint8_t* down, const float* s_down, int F,
+                  float eps, float* Y, void* workspace, size_t workspace_bytes, void* stream) {
+  const bool gated = gate != nullptr || s_gate != nullptr;
   if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
   if (M < 0 || !valid_nk(F, D) || !valid_nk(D, F) || F == 0) return BL_ERR_SHAPE;
   if (M == 0) return BL_OK;
-  if (!X || !up || !s_up || !down || !s_down || !Y || !workspace) return BL_ERR_ARG;
+  if (!X || !up || !s_up || !down || !s_down || !Y || !workspace || (gated && (!gate || !s_gate)))
+    return BL_ERR_ARG;
   if (!aligned16(X) || !aligned16(up) || !aligned16(down) || !aligned16(Y) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(s_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u))
+      (reinterpret_cast<uintptr_t>(s_up) & 3u) || (reinterpret_cast<uintptr_t>(s_down) & 3u) ||
+      (gated && (!aligned16(gate) || (reinterpret_cast<uintptr_t>(s_gate) & 3u))))
     return BL_ERR_ALIGN;
-  if (workspace_bytes < bitlinear_workspace_bytes(BL_OP_FFN, M, F, D)) return BL_ERR_WORKSPACE;
+  if (workspace_bytes < bitlinear_workspace_bytes(gated ? BL_OP_FFN_GATED : BL_OP_FFN, M, F, D))
+    return BL_ERR_WORKSPACE;
   if (bl_status s = check_device(); s != BL_OK) return s;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FfnLayout L = ffn_layout(M, D, F);
-  if (M >= kGemmMinTokens) {
-    void* ax = at<void>(workspace, L.qx);
-    float* mx = at<float>(workspace, L.mx);
-    float* h = at<float>(workspace, L.h);
-    void* ah = at<void>(workspace, L.qh);
-    float* mh = at<float>(workspace, L.mh);
-    WsHeader* hdr = static_cast<WsHeader*>(workspace);
-    if (launch_quant(X, x_dtype, M, D, eps, QLayout::kPairF16, ax, mx, nullptr, nullptr, true, st) != cudaSuccess ||
-        launch_gemm(make_gemm(M, D, up, s_up, F, ax, mx, h, nullptr, true, at<int32_t>(workspace, L.accw)), hdr,
-                    true, st) != cudaSuccess ||
-        launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kPairF16, ah, mh, nullptr, nullptr, true, st) !=
-            cudaSuccess)
-      return BL_ERR_CUDA;
-    return from_cuda(launch_gemm(make_gemm(M, F, down, s_down, D, ah, mh, Y, nullptr, false,
-                                           at<int32_t>(workspace, L.accw)),
-                                 hdr, true, st));
-  }
-  int8_t* qx = at<int8_t>(workspace, L.qx);
+  const FfnLayout L = ffn_layout(M, D, F, gated);
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
   float* mx = at<float>(workspace, L.mx);
   float* h = at<float>(workspace, L.h);
-  int8_t* qh = at<int8_t>(workspace, L.qh);
   float* mh = at<float>(workspace, L.mh);
+  float* g = gated ? at<float>(workspace, L.g) : nullptr;
+  if (M >= kGemmMinTokens) {
+    void* ax = at<void>(workspace, L.qx);
+    void* ah = at<void>(workspace, L.qh);
+    int32_t* accw = at<int32_t>(workspace, L.accw);
+    if (launch_quant(X, x_dtype, M, D, eps, QLayout::kPairF16, ax, mx, nullptr, nullptr, true, st) != cudaSuccess)
+      return BL_ERR_CUDA;
+    if (gated) {
+      if (launch_gemm(make_gemm(M, D, gate, s_gate, F, ax, mx, g, nullptr, true, accw), hdr, true, st) !=
+          cudaSuccess)
+        return BL_ERR_CUDA;
+      GemmProblem gu = make_gemm(M, D, up, s_up, F, ax, mx, h, nullptr, false, accw);
+      gu.mul = g;
+      if (launch_gemm(gu, hdr, true, st) != cudaSuccess) return BL_ERR_CUDA;
+    } else if (launch_gemm(make_gemm(M, D, up, s_up, F, ax, mx, h, nullptr, true, accw), hdr, true, st) !=
+               cudaSuccess) {
+      return BL_ERR_CUDA;
+    }
+    if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kPairF16, ah, mh, nullptr, nullptr, true, st) !=
+        cudaSuccess)
+      return BL_ERR_CUDA;
+    return from_cuda(launch_gemm(make_gemm(M, F, down, s_down, D, ah, mh, Y, nullptr, false, accw), hdr, true, st));
+  }
+  int8_t* qx = at<int8_t>(workspace, L.qx);
+  int8_t* qh = at<int8_t>(workspace, L.qh);
   if (launch_quant(X, x_dtype, M, D, eps, QLayout::kRowMajorI8, qx, mx, nullptr, nullptr, true, st) != cudaSuccess)
     return BL_ERR_CUDA;
+  if (gated) {
+    GemvProblem pg = make_problem(M, D, gate, s_gate, F, g, nullptr);
+    pg.q = qx;
+    pg.m = mx;
+    pg.epi = Epi::kRelu2;
+    if (launch_gemv(pg, hdr, true, st) != cudaSuccess) return BL_ERR_CUDA;
+  }
   GemvProblem pu = make_problem(M, D, up, s_up, F, h, nullptr);
   pu.q = qx;
   pu.m = mx;
-  pu.epi = Epi::kRelu2;
-  if (launch_gemv(pu, static_cast<WsHeader*>(workspace), true, st) != cudaSuccess) return BL_ERR_CUDA;
+  if (gated) pu.mul = g;
+  else pu.epi = Epi::kRelu2;
+  if (launch_gemv(pu, hdr, true, st) != cudaSuccess) return BL_ERR_CUDA;
   if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kRowMajorI8, qh, mh, nullptr, nullptr, true, st) !=
       cudaSuccess)
     return BL_ERR_CUDA;
   GemvProblem pd = make_problem(M, F, down, s_down, D, Y, nullptr);
   pd.q = qh;
   pd.m = mh;
-  return from_cuda(launch_gemv(pd, static_cast<WsHeader*>(workspace), true, st));
+  return from_cuda(launch_gemv(pd, hdr, true, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+bl_status bitlinear_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
+                        const uint8_t* down, const float* s_down, int F, float eps, float* Y, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  return run_ffn(X, x_dtype, M, D, up, s_up, nullptr, nullptr, down, s_down, F, eps, Y, workspace, workspace_bytes,
+                 stream);
+}
+
+bl_status bitlinear_ffn_gated(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
+                              const uint8_t* gate, const float* s_gate, const uint8_t* down, const float* s_down,
+                              int F, float eps, float* Y, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!gate || !s_gate) return BL_ERR_ARG;
+  return run_ffn(X, x_dtype, M, D, up, s_up, gate, s_gate, down, s_down, F, eps, Y, workspace, workspace_bytes,
+                 stream);
 }
 
 bl_status bitlinear_unpack(const uint8_t* packed, int N, int K, int8_t* t, void* stream) {

@@ -98,6 +98,7 @@ struct GemmParams {
   int M, N, K;
   int splits;            // K is cut into this many parts, one work unit each
   int32_t* acc_ws;       // splits > 1: [M][N] int32 partial-sum target (zeroed)
+  const float* mul;      // [M][N] or null: y = fp32(y * mul)
   const float* m;        // [M] per-token scales
   const float* s_w;      // [1]
   float* Y;              // [M][N]
@@ -226,7 +227,7 @@ __device__ __forceinline__ uint32_t pair_word(uint32_t w_lo, uint32_t w_hi) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
-template <class C, bool RELU2, bool ACC, bool SPLIT>
+template <class C, bool RELU2, bool ACC, bool SPLIT, bool MUL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_act, const __grid_constant__ CUtensorMap tm_codes,
                    const GemmParams p) {
@@ -454,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* yp = p.Y + static_cast<size_t>(tok0) * p.N + n;
         int32_t* ap = ACC ? p.acc + static_cast<size_t>(tok0) * p.N + n : nullptr;
+        const float* mp = MUL ? p.mul + static_cast<size_t>(tok0) * p.N + n : nullptr;
         const int jmax = min(32, p.M - tok0);
         if (jmax == 32 && n_ok) {
 #pragma unroll
@@ -461,6 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float accf = __uint_as_float(v[j]);
             float y = __fmul_rn(accf, __shfl_sync(0xffffffffu, my_c, j));
             if constexpr (RELU2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
+            if constexpr (MUL) {
+              y = __fmul_rn(y, *mp);
+              mp += p.N;
+            }
             *yp = y;
             yp += p.N;
             if constexpr (ACC) {
@@ -475,11 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float y = __fmul_rn(accf, __shfl_sync(0xffffffffu, my_c, j));
             if constexpr (RELU2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
             if (j < jmax && n_ok) {
+              if constexpr (MUL) y = __fmul_rn(y, *mp);
               *yp = y;
               if constexpr (ACC) *ap = __float2int_rn(accf);
             }
             yp += p.N;
             if constexpr (ACC) ap += p.N;
+            if constexpr (MUL) mp += p.N;
           }
         }
       }
@@ -502,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) split_finalize_kernel(const int32_t* __restrict__ acc_ws, int M, int N,
                                                              const float* __restrict__ m,
                                                              const float* __restrict__ s_w, float* __restrict__ Y,
-                                                             int32_t* __restrict__ acc, int relu2) {
+                                                             int32_t* __restrict__ acc, int relu2,
+                                                             const float* __restrict__ mul) {
   pdl_wait();
   pdl_trigger();
   const int tok = blockIdx.y;
@@ -512,6 +521,7 @@ __global__ void __launch_bounds__(256) split_finalize_kernel(const int32_t* __re
     const int v = acc_ws[o];
     float y = __fmul_rn(static_cast<float>(v), c);
     if (relu2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
+    if (mul != nullptr) y = __fmul_rn(y, mul[o]);
     Y[o] = y;
     if (acc != nullptr) acc[o] = v;
   }
@@ -574,6 +584,7 @@ cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStr
   p.K = g.K;
   p.splits = std::max(1, splits);
   p.acc_ws = g.acc_ws;
+  p.mul = g.mul;
   p.m = g.m;
   p.s_w = g.s_w;
   p.Y = g.Y;
@@ -582,11 +593,15 @@ cudaError_t launch_cfg(const GemmProblem& g, WsHeader* status, bool pdl, cudaStr
   const int tiles = ((g.N + kTileN - 1) / kTileN) * ((g.M + C::kTileM - 1) / C::kTileM);
   const int grid = std::max(1, std::min(tiles * p.splits, sm_count()));
   const size_t smem = C::smem_bytes();
-  auto kern = p.splits > 1 ? gemm_tc_kernel<C, false, false, true>
-               : g.relu2 ? (g.acc != nullptr ? gemm_tc_kernel<C, true, true, false>
-                                              : gemm_tc_kernel<C, true, false, false>)
-                         : (g.acc != nullptr ? gemm_tc_kernel<C, false, true, false>
-                                              : gemm_tc_kernel<C, false, false, false>);
+  // epilogue variants in use: plain, ReLU^2 (FFN up), times a second operand
+  // (gated FFN up), each with or without the integer accumulators; split-K
+  // runs apply the epilogue in split_finalize_kernel
+  auto kern = p.splits > 1 ? gemm_tc_kernel<C, false, false, true, false>
+               : g.mul != nullptr ? gemm_tc_kernel<C, false, false, false, true>
+               : g.relu2 ? (g.acc != nullptr ? gemm_tc_kernel<C, true, true, false, false>
+                                              : gemm_tc_kernel<C, true, false, false, false>)
+                         : (g.acc != nullptr ? gemm_tc_kernel<C, false, true, false, false>
+                                              : gemm_tc_kernel<C, false, false, false, false>);
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -642,7 +657,7 @@ cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaSt
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       return cudaLaunchKernelEx(&cfg, split_finalize_kernel, static_cast<const int32_t*>(g.acc_ws), g.M, g.N, g.m,
-                                g.s_w, g.Y, g.acc, g.relu2 ? 1 : 0);
+                                g.s_w, g.Y, g.acc, g.relu2 ? 1 : 0, g.mul);
     }
     return launch_cfg<CfgNarrow>(g, status, pdl, st, 1);
   }

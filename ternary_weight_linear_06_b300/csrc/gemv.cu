@@ -67,6 +67,7 @@ struct DevProb {
   const float* s_w;
   float* Y;
   int32_t* acc;
+  const float* mul;       // [M][N] or null: y = fp32(y * mul)
   int N, K, M;
   int epi;
   int lpr;                // lanes per row
@@ -219,6 +220,7 @@ __device__ __forceinline__ void run_span(const DevProb& P, const Span<MT>& S, co
         float y = __fmul_rn(static_cast<float>(accv), S.c[t]);
         if (P.epi == static_cast<int>(Epi::kRelu2)) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
         const size_t o = static_cast<size_t>(tok) * P.N + row;
+        if (P.mul != nullptr) y = __fmul_rn(y, P.mul[o]);
         P.Y[o] = y;
         if (P.acc != nullptr) P.acc[o] = accv;
       }
@@ -413,6 +415,7 @@ DevProb to_dev(const GemvProblem& p) {
   d.s_w = p.s_w;
   d.Y = p.Y;
   d.acc = p.acc;
+  d.mul = p.mul;
   d.N = p.N;
   d.K = p.K;
   d.M = p.M;

@@ -53,6 +53,7 @@ struct GemvProblem {
   float* Y;              // [M][N] fp32 (h = relu2(y) for kRelu2)
   int32_t* acc;          // [M][N] or null
   Epi epi;
+  const float* mul;      // [M][N] or null: y = fp32(y * mul) (the gated FFN's up projection)
 };
 constexpr int kGemvMaxBatch = 128;
 // One problem (M <= 4 per launch; more tokens take several launches).
@@ -70,6 +71,7 @@ struct GemmProblem {
   float* Y;              // [M][N]
   int32_t* acc;          // [M][N] or null
   bool relu2;            // FFN up: write h = relu(y)^2
+  const float* mul;      // [M][N] or null: y = fp32(y * mul) (the gated FFN's up projection)
   int32_t* acc_ws;       // [M][N] int32 scratch for a split-K run, or null (no split)
 };
 // How many K parts a GEMM of these sizes is cut into (1: no split). Split runs

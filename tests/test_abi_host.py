@@ -74,6 +74,13 @@ def test_host_argument_checks_fail_before_launch():
     assert lib.bitlinear_forward(None, 0, 3, 64, None, None, 0, 1e-5, None, None, None, 0, None) == _lib.BL_OK
     assert lib.bitlinear_quant_act(None, 0, 0, 64, 1e-5, None, None, None) == _lib.BL_OK
     assert lib.bitlinear_workspace_status(None, None) == _lib.BL_ERR_ARG
+    # gated FFN: the gate is required; workspace sized for the gate buffer
+    assert lib.bitlinear_ffn_gated(p, 0, 2, 64, p, p, None, p, p, p, 128, 1e-5, p, p, 1 << 20, None) == _lib.BL_ERR_ARG
+    need = lib.bitlinear_workspace_bytes(_lib.BL_OP_FFN_GATED, 2, 128, 64)
+    assert need > lib.bitlinear_workspace_bytes(_lib.BL_OP_FFN, 2, 128, 64)
+    assert lib.bitlinear_ffn_gated(p, 0, 2, 64, p, p, p, p, p, p, 128, 1e-5, p, p, need - 256, None) == \
+        _lib.BL_ERR_WORKSPACE
+    assert lib.bitlinear_ffn_gated(p, 0, 2, 64, p, p, p + 4, p, p, p, 128, 1e-5, p, p, need, None) == _lib.BL_ERR_ALIGN
     # tensor-core operand form
     assert lib.bitlinear_quant_act_tc(p, 0, 2, 96, 1e-5, p, p, None) == _lib.BL_ERR_SHAPE
     assert lib.bitlinear_quant_act_tc(p, 0, 2, 64, 1e-5, p + 8, p, None) == _lib.BL_ERR_ALIGN

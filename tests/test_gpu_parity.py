@@ -464,3 +464,39 @@ def test_large_ffn_shapes_sampled_rows(shape, M):
     # tokens) and with 128/192/256-token tiles (512 tokens)
     K, N = WL.SHAPES_70B[shape]
     _check_sampled(WL.large_weights(shape), WL.student_t(M, K, seed=M + K), 23)
+
+
+# -------------------------------------------------------------- gated FFN
+@pytest.mark.parametrize("M", [1, 4, 16, 200])
+def test_gated_ffn_all_paths(M):
+    # 1 and 4 tokens: GEMV; 16: split-K GEMM; 200: tiled GEMM
+    D, F = 256, 640
+    Wu = WL.gaussian_weights(F, D, 0.02, seed=110 + M, outlier_frac=0.001)
+    Wg = WL.gaussian_weights(F, D, 0.02, seed=120 + M, outlier_frac=0.001)
+    Wd = WL.gaussian_weights(D, F, 0.02, seed=130 + M, outlier_frac=0.001)
+    X = WL.prefill_activations(M, D, seed=140 + M)
+    up, s_up = BL.pack(dev(Wu))
+    gate, s_gate = BL.pack(dev(Wg))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sg, tg = O.pack_weights(Wg)
+    _, sd, td = O.pack_weights(Wd)
+    Y = BL.ffn_gated(dev(X), up, s_up, gate, s_gate, down, s_down)
+    Y_ref, _ = O.ffn_gated(X, tu, su, tg, sg, td, sd)
+    assert_y(host(Y), Y_ref)
+    assert BL.workspace_status() == 0
+
+
+def test_gated_ffn_2b_shapes_split_k():
+    D, F, M = 2560, 6912, 12
+    Wu, Wg, Wd = WL.decode_weights("up", 6), WL.decode_weights("up", 7), WL.decode_weights("down", 6)
+    X = WL.student_t(M, D, seed=150)
+    up, s_up = BL.pack(dev(Wu))
+    gate, s_gate = BL.pack(dev(Wg))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sg, tg = O.pack_weights(Wg)
+    _, sd, td = O.pack_weights(Wd)
+    Y = BL.ffn_gated(dev(X), up, s_up, gate, s_gate, down, s_down)
+    Y_ref, _ = O.ffn_gated(X, tu, su, tg, sg, td, sd)
+    assert_y(host(Y), Y_ref)

@@ -311,6 +311,36 @@ def test_relu2_and_ffn_composition():
     assert qh.min() >= 0
 
 
+def test_gated_ffn_sign_flip_and_zero_gate():
+    # Flipping the sign of the gate weights flips the sign of every gate output
+    # exactly (the quantizers are odd), so for each element exactly one of the
+    # two gated h values is ReLU^2(+-y_gate) * y_up and the other is +-0; their
+    # sum is fp32(fp32(y_gate^2) * y_up), computed here from y alone.
+    rng = np.random.default_rng(9)
+    Wu = WL.gaussian_weights(48, 64, 0.02, seed=10)
+    Wg = WL.gaussian_weights(48, 64, 0.02, seed=11)
+    Wd = WL.gaussian_weights(64, 48, 0.02, seed=12)
+    X = rng.standard_normal((6, 64)).astype(np.float32)
+    _, su, tu = O.pack_weights(Wu)
+    _, sg, tg = O.pack_weights(Wg)
+    _, sgn, tgn = O.pack_weights(-Wg)
+    assert sgn == sg and np.array_equal(tgn, -tg)
+    _, sd, td = O.pack_weights(Wd)
+    _, h1 = O.ffn_gated(X, tu, su, tg, sg, td, sd)
+    _, h2 = O.ffn_gated(X, tu, su, tgn, sgn, td, sd)
+    y_up = O.forward(X, tu, su)[0].astype(np.float64)
+    y_g = O.forward(X, tg, sg)[0].astype(np.float64)
+    sq = np.array(y_g * y_g, np.float32).astype(np.float64)          # fp32(y_g^2), exact product in fp64
+    expect = np.array(sq * y_up, np.float32)                           # one fp32 rounding of the product
+    np.testing.assert_array_equal((h1.astype(np.float64) + h2.astype(np.float64)).astype(np.float32), expect)
+    assert np.all((h1 == 0) | (h2 == 0))
+    # where the gate is not positive, h is a zero (of either sign) whatever up is
+    assert np.all(h1[y_g <= 0] == 0)
+    # a gate equal to up gives h = ReLU(y)^2 * y: non-negative, zero for y <= 0
+    _, h3 = O.ffn_gated(X, tu, su, tu, su, td, sd)
+    assert np.all(h3 >= 0) and np.all(h3[y_up <= 0] == 0)
+
+
 def test_tie_count_diagnostic():
     s = np.float32(1.0)
     W = np.array([[0.5, np.nextafter(np.float32(0.5), np.float32(1)), 0.3, -0.5]], np.float32)
