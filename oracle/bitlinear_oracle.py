@@ -40,14 +40,24 @@ Readings where the pages are silent (each repeated in the design notes):
     holds k = 4b + j in bits [2j, 2j+1] (little end first).
   * FFN: ungated up -> ReLU^2 -> requant (same eps) -> down; no norm between.
   * gated FFN: h = fp32(fp32(ReLU(gate)^2) * up), then requant and down.
+  * SubLN is an RMSNorm with a per-feature gain g and no bias, applied to the
+    input of a BitLinear before its activation quantization:
+    n_ik = x_ik * g_k * r_i, r_i = 1 / sqrt(mean_k x_ik^2 + eps_norm),
+    eps_norm = 1e-5. In the FFN it sits on the block input and on h before
+    the down projection. Absmax codes do not change when a row is multiplied
+    by the positive factor r_i, so the codes are taken from u = fp32(x * g)
+    and r_i goes into the per-token scale: m_i = fp32(max(max|u|, eps) * r_i).
+    r_i is computed in fp64 from the exact sum of squares.
 """
 from __future__ import annotations
 
+import math
 from fractions import Fraction
 
 import numpy as np
 
 EPS = np.float32(1e-5)
+EPS_NORM = np.float32(1e-5)
 QB = 127
 FLT_MAX = Fraction(int(np.finfo(np.float32).max))
 
@@ -57,6 +67,7 @@ __all__ = [
     "ternarize", "pack_codes", "unpack_codes", "pack_weights",
     "bf16_bits_to_f32", "quant_act", "int_matmul", "dequant", "forward",
     "forward_packed", "relu2", "ffn", "ffn_gated", "tie_count",
+    "EPS_NORM", "rms_factor", "rmsnorm_quant", "forward_rmsnorm", "ffn_subln",
 ]
 
 
@@ -262,3 +273,62 @@ def ffn_gated(X, t_up, s_up, t_gate, s_gate, t_down, s_down, eps=EPS):
     y_gate = forward(X, t_gate, s_gate, eps)[0]
     h = (relu2(y_gate) * y_up).astype(np.float32)
     return forward(h, t_down, s_down, eps)[0], h
+
+
+# --------------------------------------------------------------------------
+# SubLN: RMSNorm before the activation quantization
+#   [P1 §2 架构, 归一化 and 偏置移除], [P2 架构上的关键修改, 归一化 row],
+#   [P3 模型架构, 组件兼容性: RMSNorm]
+# --------------------------------------------------------------------------
+def rms_factor(X, eps_norm=EPS_NORM) -> np.ndarray:
+    """r_i = 1 / sqrt(S_i / K + eps_norm) in fp64, S_i = sum_k x_ik^2.
+
+    Each square of an fp32 value is exact in fp64, and math.fsum rounds their
+    exact sum once, so S_i is the correctly rounded sum. The division, the
+    addition of eps_norm (an fp32 value), the square root and the reciprocal
+    are then fp64 operations, each rounded once, in that order."""
+    X = _f32(X)
+    M, K = X.shape
+    e = float(np.float32(eps_norm))
+    r = np.empty(M, np.float64)
+    for i in range(M):
+        S = math.fsum((X[i].astype(np.float64) ** 2).tolist())
+        r[i] = 1.0 / math.sqrt(S / K + e)
+    return r
+
+
+def rmsnorm_quant(X, g=None, eps_norm=EPS_NORM, eps=EPS):
+    """RMSNorm (gain g [K], no bias) followed by the per-token absmax quant.
+
+    Codes come from u = fp32(x * g) (u = x without a gain) because absmax
+    codes ignore the positive per-token factor r_i; the factor goes into the
+    scale: (q, m_u) = quant_act(u); m_i = fp32(fp64(m_u_i) * r_i).
+    Returns (q int8 [M, K], m fp32 [M])."""
+    X = _f32(X)
+    u = X if g is None else (X * _f32(g)[None, :]).astype(np.float32)
+    q, m_u = quant_act(u, eps)
+    r = rms_factor(X, eps_norm)
+    m = (m_u.astype(np.float64) * r).astype(np.float32)
+    return q, m
+
+
+def forward_rmsnorm(X, t, s_w, g=None, eps_norm=EPS_NORM, eps=EPS):
+    """BitLinear forward on RMSNorm(X): returns (Y, acc, q, m) like forward()."""
+    q, m = rmsnorm_quant(X, g, eps_norm, eps)
+    acc = int_matmul(q, t)
+    return dequant(acc, s_w, m), acc, q, m
+
+
+def ffn_subln(X, t_up, s_up, t_down, s_down, g_in=None, g_sub=None, t_gate=None, s_gate=None,
+              eps_norm=EPS_NORM, eps=EPS):
+    """FFN block with SubLN: RMSNorm(g_in) on X, up (and gate) on that one
+    quantization, ReLU^2 (times up when gated), RMSNorm(g_sub) on h, down.
+    Returns (Y, h)."""
+    q, m = rmsnorm_quant(X, g_in, eps_norm, eps)
+    y_up = dequant(int_matmul(q, t_up), s_up, m)
+    if t_gate is None:
+        h = relu2(y_up)
+    else:
+        y_gate = dequant(int_matmul(q, t_gate), s_gate, m)
+        h = (relu2(y_gate) * y_up).astype(np.float32)
+    return forward_rmsnorm(h, t_down, s_down, g_sub, eps_norm, eps)[0], h

@@ -345,3 +345,113 @@ def test_tie_count_diagnostic():
     s = np.float32(1.0)
     W = np.array([[0.5, np.nextafter(np.float32(0.5), np.float32(1)), 0.3, -0.5]], np.float32)
     assert O.tie_count(W, s) == 3
+
+
+# ----------------------------------------------------------------- SubLN RMSNorm
+def test_rmsnorm_constant_rows_closed_form():
+    # x = c in every column: mean x^2 = c^2, so every normalized value is
+    # sign(c) * |c| / sqrt(c^2 + e); every code is +-127 and the scale is that
+    # magnitude. A sum in place of the mean (1/sqrt(K) off), eps outside the
+    # root, or a missing root each miss it by far more than an fp32 step.
+    K = 256
+    for c in (3.0, -0.75, 1024.0):
+        for e in (0.0, 0.5, 1e-5):
+            X = np.full((1, K), c, np.float32)
+            q, m = O.rmsnorm_quant(X, eps_norm=e)
+            assert np.all(q == (127 if c > 0 else -127))
+            want = abs(c) / math.sqrt(c * c + float(np.float32(e)))
+            assert abs(float(m[0]) - want) <= 2.0 ** -23 * want, (c, e, m[0], want)
+
+
+def test_rmsnorm_one_hot_gain():
+    # A gain that keeps one column j: u has one non-zero entry, so its code is
+    # +-127 (sign of x_j * gain) and every other code is 0. The scale is
+    # |x_j * gain| / sqrt(rms(x)^2 + e): the statistic is over x, not over the
+    # gained row (which would give sqrt(K) / |gain| instead).
+    rng = np.random.default_rng(21)
+    K, j, gam, e = 128, 37, np.float32(-2.5), 0.25
+    X = rng.standard_normal((5, K)).astype(np.float32)
+    g = np.zeros(K, np.float32)
+    g[j] = gam
+    q, m = O.rmsnorm_quant(X, g, eps_norm=e)
+    want_q = np.zeros_like(q)
+    want_q[:, j] = np.where(X[:, j] * gam > 0, 127, -127)
+    np.testing.assert_array_equal(q, want_q)
+    rms = np.linalg.norm(X.astype(np.float64), axis=1) / math.sqrt(K)
+    want = np.abs(X[:, j].astype(np.float64) * float(gam)) / np.sqrt(rms ** 2 + e)
+    np.testing.assert_allclose(m.astype(np.float64), want, rtol=2.5e-7)
+
+
+def test_rmsnorm_scale_invariance_without_eps():
+    # With eps_norm = 0 the norm removes any per-row factor; for powers of two
+    # every step is exact, so codes and scales are bit-identical.
+    rng = np.random.default_rng(24)
+    X = rng.standard_normal((7, 320)).astype(np.float32)
+    g = rng.uniform(-2, 2, 320).astype(np.float32)
+    q0, m0 = O.rmsnorm_quant(X, g, eps_norm=0.0)
+    for k in (-6, -1, 3, 20):
+        q, m = O.rmsnorm_quant((X * np.float32(2.0 ** k)).astype(np.float32), g, eps_norm=0.0)
+        np.testing.assert_array_equal(q, q0)
+        np.testing.assert_array_equal(m.view(np.uint32), m0.view(np.uint32))
+    # eps_norm > 0 does change the scale of a small row (sqrt(rms^2 + e) > rms)
+    _, m_small = O.rmsnorm_quant((X * np.float32(2.0 ** -6)).astype(np.float32), g, eps_norm=0.5)
+    _, m_unit = O.rmsnorm_quant(X, g, eps_norm=0.5)
+    assert np.all(m_small < m_unit)
+
+
+def test_rmsnorm_forward_matches_literal_normalize_then_quantize():
+    # The definition read literally, in fp64: n = x * g / sqrt(mean x^2 + e),
+    # codes rint(127 n / max|n|), Y = s_w * (codes . t) * max|n| / 127. The
+    # oracle takes the codes from fp32(x * g) instead: they may differ only
+    # where 127 n / max|n| lies within fp32 rounding of a half-integer, and the
+    # oracle's scale m must equal max|n| up to that rounding.
+    rng = np.random.default_rng(22)
+    M, K, N, e = 48, 512, 40, 1e-5
+    X = (rng.standard_normal((M, K)) * rng.uniform(0.1, 30, (M, 1))).astype(np.float32)
+    g = rng.uniform(-1.5, 1.5, K).astype(np.float32)
+    _, s_w, t = O.pack_weights(WL.gaussian_weights(N, K, 0.02, seed=23))
+    Y, acc, q, m = O.forward_rmsnorm(X, t, s_w, g, eps_norm=e)
+    x = X.astype(np.float64)
+    n = x * g.astype(np.float64) / np.sqrt((x * x).mean(axis=1, keepdims=True) + float(np.float32(e)))
+    amax = np.abs(n).max(axis=1)
+    v = 127.0 * n / amax[:, None]
+    q_lit = np.clip(np.rint(v), -128, 127)
+    near_tie = np.abs(np.abs(v - np.floor(v)) - 0.5) < 1e-4
+    assert np.all((q == q_lit) | near_tie)
+    np.testing.assert_allclose(m.astype(np.float64), amax, rtol=2.5e-7)
+    y_lit = float(s_w) * acc.astype(np.float64) * amax[:, None] / 127.0
+    nz = acc != 0
+    assert np.all(np.abs(Y[nz] - y_lit[nz]) <= 6e-7 * np.abs(y_lit[nz]))
+    assert np.all(Y[~nz] == 0)
+
+
+def test_ffn_subln_norms_remove_scales():
+    # eps_norm = 0: the input norm makes Y independent of a power-of-two scale
+    # of X, and the norm on h makes it independent of a power-of-two scale of
+    # s_up (h scales by 16 ungated, by 4 gated) or of s_gate. Without the norm
+    # on h the second check fails: the plain FFN is not invariant.
+    rng = np.random.default_rng(25)
+    D, F, M = 64, 96, 5
+    X = rng.standard_normal((M, D)).astype(np.float32)
+    _, su, tu = O.pack_weights(WL.gaussian_weights(F, D, 0.02, seed=26))
+    _, sg, tg = O.pack_weights(WL.gaussian_weights(F, D, 0.02, seed=27))
+    _, sd, td = O.pack_weights(WL.gaussian_weights(D, F, 0.02, seed=28))
+    g_in = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    g_sub = rng.uniform(-1.5, 1.5, F).astype(np.float32)
+    four, two = np.float32(4), np.float32(2)
+    for gated in (False, True):
+        kw = dict(g_in=g_in, g_sub=g_sub, eps_norm=0.0)
+        if gated:
+            kw.update(t_gate=tg, s_gate=sg)
+        Y0, _ = O.ffn_subln(X, tu, su, td, sd, **kw)
+        Y1, _ = O.ffn_subln((X * np.float32(8)).astype(np.float32), tu, su, td, sd, **kw)
+        Y2, _ = O.ffn_subln(X, tu, su * four, td, sd, **kw)
+        np.testing.assert_array_equal(Y1.view(np.uint32), Y0.view(np.uint32))
+        np.testing.assert_array_equal(Y2.view(np.uint32), Y0.view(np.uint32))
+        if gated:
+            kw.update(s_gate=sg * two)
+            Y3, _ = O.ffn_subln(X, tu, su, td, sd, **kw)
+            np.testing.assert_array_equal(Y3.view(np.uint32), Y0.view(np.uint32))
+    P0, _ = O.ffn(X, tu, su, td, sd)
+    P2, _ = O.ffn(X, tu, su * four, td, sd)
+    assert not np.array_equal(P0, P2)
