@@ -26,6 +26,14 @@
  *   y_in   = fp32(float(acc_in) * fp32(fp32(s_w * m_i) / 127))
  *   FFN    : h = y_up > 0 ? fp32(y_up * y_up) : 0, requantized as above,
  *            then the down projection (no gate, no norm in between).
+ *   RMSNorm: (the *_rmsnorm / *_subln calls) with gain g [K] (null: 1) and
+ *            r_i = 1 / sqrt(S_i / K + eps_norm), S_i = sum_k x_ik^2, in fp64:
+ *            codes from u_ik = fp32(x_ik * g_k) as above (absmax codes do not
+ *            change under the positive factor r_i), m_i = fp32(max(max_k
+ *            |u_ik|, eps) * r_i). S_i is summed with compensated fp32
+ *            arithmetic, far below an fp32 step from exact, so m_i matches
+ *            the exact-sum value except within that distance of an fp32
+ *            rounding boundary (then it is one step off).
  *
  * Conventions for every call:
  *   - All tensors are row-major, on the current CUDA device, allocated and
@@ -273,6 +281,46 @@ BL_API bl_status bitlinear_ffn_gated(const void* X, int x_dtype, int M, int D,
                               const uint8_t* up, const float* s_up,
                               const uint8_t* gate, const float* s_gate,
                               const uint8_t* down, const float* s_down, int F, float eps,
+                              float* Y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * SubLN's RMSNorm fused into the per-token absmax quantization ("BitNet b1.58
+ * 2B4T Technical Report", section 2 (架构): a sub-layer norm, norm layers
+ * without bias; "BitNet解读", 模型架构 / 组件兼容性: RMSNorm as the norm).
+ *   X        [M, K] fp32 or bf16, device.  g [K] fp32 gain, device, or NULL
+ *            (unit gain). eps_norm > 0 and finite (1e-5 in the reference
+ *            configuration); eps as bitlinear_quant_act.
+ *   q        [M, K] int8, device, output: the codes of fp32(x * g).
+ *   m        [M] fp32, device, output: the token scales with the norm factor
+ *            folded in (the RMSNorm definition at the top of this file), ready
+ *            for bitlinear_forward_q8 or a BL_DTYPE_I8 batch problem.
+ * S_i must be finite in fp32 (|x| below about 1e19).
+ */
+BL_API bl_status bitlinear_rmsnorm_quant(const void* X, int x_dtype, int M, int K, const float* g, float eps_norm,
+                                  float eps, int8_t* q, float* m, void* stream);
+
+/*
+ * BitLinear forward on RMSNorm(X): Y = dequant(quant(RMSNorm_g(X)) . T^T).
+ * Arguments as bitlinear_forward plus g and eps_norm as
+ * bitlinear_rmsnorm_quant; the workspace is sized with BL_OP_FORWARD.
+ */
+BL_API bl_status bitlinear_forward_rmsnorm(const void* X, int x_dtype, int M, int K, const float* g,
+                                    float eps_norm, const uint8_t* packed, const float* s_w, int N,
+                                    float eps, float* Y, int32_t* acc,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FFN block with SubLN: the input X is RMS-normalized (gain g_in) and
+ * quantized once for up (and gate); h = ReLU^2(y_up), or fp32(ReLU^2(y_gate)
+ * * y_up) when gate is given, is RMS-normalized (gain g_sub) and quantized
+ * for down. gate and s_gate are both NULL (ungated) or both set; g_in, g_sub
+ * NULL mean unit gains. Other arguments as bitlinear_ffn_gated; the workspace
+ * is sized with BL_OP_FFN_GATED when gated, BL_OP_FFN otherwise.
+ */
+BL_API bl_status bitlinear_ffn_subln(const void* X, int x_dtype, int M, int D, const float* g_in,
+                              const uint8_t* up, const float* s_up,
+                              const uint8_t* gate, const float* s_gate, const float* g_sub,
+                              const uint8_t* down, const float* s_down, int F, float eps_norm, float eps,
                               float* Y, void* workspace, size_t workspace_bytes, void* stream);
 
 /*

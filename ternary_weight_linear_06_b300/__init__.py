@@ -8,6 +8,7 @@ runs in the library's CUDA kernels; there is no CPU or PyTorch fallback.
     packed, s_w = pack(W)                    # W [N, K] fp32 on the GPU
     Y = forward(X, packed, s_w)              # X [M, K] fp32 or bf16
     Y = ffn(X, up, s_up, down, s_down)       # up->ReLU^2->requant->down
+    Y = forward_rmsnorm(X, packed, s_w, g)   # RMSNorm fused into the quantization
 """
 from __future__ import annotations
 
@@ -19,10 +20,12 @@ from ._lib import (BL_DTYPE_BF16, BL_DTYPE_F32, BL_DTYPE_I8, BL_MAX_BATCH, BL_OP
                    BL_OP_FORWARD_BATCH, BL_OP_PACK, BitLinearError, ForwardDesc, check)
 
 EPS = 1e-5
+EPS_NORM = 1e-5
 
 __all__ = ["pack", "quant_act", "quant_act_tc", "forward", "forward_batch", "forward_q8", "forward_tc",
-           "forward_noalloc", "ffn", "ffn_gated", "unpack", "workspace_bytes", "workspace_status",
-           "Workspace", "BitLinearError", "EPS", "library_path"]
+           "forward_noalloc", "ffn", "ffn_gated", "rmsnorm_quant", "forward_rmsnorm", "ffn_subln", "unpack",
+           "workspace_bytes", "workspace_status", "Workspace", "BitLinearError", "EPS", "EPS_NORM",
+           "library_path"]
 
 
 def library_path() -> str:
@@ -275,6 +278,76 @@ def ffn_gated(X: torch.Tensor, up: torch.Tensor, s_up: torch.Tensor, gate: torch
     check(_lib.lib().bitlinear_ffn_gated(_ptr(X), _x_dtype(X), M, D, _ptr(up), _ptr(s_up), _ptr(gate), _ptr(s_gate),
                                          _ptr(down), _ptr(s_down), F, eps, _ptr(Y), _ptr(ws), ws.numel(),
                                          _stream(stream)), "bitlinear_ffn_gated")
+    return Y
+
+
+def _need_gain(g: torch.Tensor | None, K: int, name: str) -> None:
+    if g is None:
+        return
+    _need_cuda(g, name, (torch.float32,))
+    if g.dim() != 1 or g.shape[0] != K:
+        raise ValueError(f"{name} must be a [{K}] gain vector, got {tuple(g.shape)}")
+
+
+def rmsnorm_quant(X: torch.Tensor, g: torch.Tensor | None = None, eps_norm: float = EPS_NORM, eps: float = EPS,
+                  stream=None):
+    """RMSNorm (gain g [K], None = 1) fused into the per-token absmax quant.
+    Returns (q int8 [M, K], m fp32 [M]) with the norm factor folded into m."""
+    _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+    M, K = X.shape
+    _need_gain(g, K, "g")
+    q = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    m = torch.empty(max(M, 4), dtype=torch.float32, device=X.device)[:M]
+    check(_lib.lib().bitlinear_rmsnorm_quant(_ptr(X), _x_dtype(X), M, K, _ptr(g), eps_norm, eps, _ptr(q), _ptr(m),
+                                             _stream(stream)), "bitlinear_rmsnorm_quant")
+    return q, m
+
+
+def forward_rmsnorm(X: torch.Tensor, packed: torch.Tensor, s_w: torch.Tensor, g: torch.Tensor | None = None,
+                    eps_norm: float = EPS_NORM, eps: float = EPS, return_acc: bool = False,
+                    out: torch.Tensor | None = None, workspace: Workspace | None = None, stream=None):
+    """Y = BitLinear(RMSNorm_g(X)), the norm fused into the activation quantization."""
+    _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+    _need_cuda(packed, "packed", (torch.uint8,))
+    _need_cuda(s_w, "s_w", (torch.float32,))
+    M, K = X.shape
+    _need_gain(g, K, "g")
+    N = packed.shape[0]
+    if packed.shape[1] * 4 != K:
+        raise ValueError(f"packed has {packed.shape[1]} bytes per row, expected K/4 = {K // 4}")
+    Y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=X.device)
+    acc = torch.empty((M, N), dtype=torch.int32, device=X.device) if return_acc else None
+    ws = _workspace(workspace, workspace_bytes(BL_OP_FORWARD, M, N, K))
+    check(_lib.lib().bitlinear_forward_rmsnorm(_ptr(X), _x_dtype(X), M, K, _ptr(g), eps_norm, _ptr(packed),
+                                               _ptr(s_w), N, eps, _ptr(Y), _ptr(acc), _ptr(ws), ws.numel(),
+                                               _stream(stream)), "bitlinear_forward_rmsnorm")
+    return (Y, acc) if return_acc else Y
+
+
+def ffn_subln(X: torch.Tensor, up: torch.Tensor, s_up: torch.Tensor, down: torch.Tensor, s_down: torch.Tensor,
+              g_in: torch.Tensor | None = None, g_sub: torch.Tensor | None = None, gate: torch.Tensor | None = None,
+              s_gate: torch.Tensor | None = None, eps_norm: float = EPS_NORM, eps: float = EPS,
+              out: torch.Tensor | None = None, workspace: Workspace | None = None, stream=None):
+    """FFN block with SubLN: RMSNorm(g_in) on X, up (and gate), ReLU^2 (times up
+    when gated), RMSNorm(g_sub) on h, down."""
+    _need_cuda(X, "X", (torch.float32, torch.bfloat16))
+    gated = gate is not None
+    if gated != (s_gate is not None):
+        raise ValueError("gate and s_gate go together")
+    for t, n in ((up, "up"), (down, "down")) + (((gate, "gate"),) if gated else ()):
+        _need_cuda(t, n, (torch.uint8,))
+    M, D = X.shape
+    F = up.shape[0]
+    if (up.shape[1] * 4 != D or down.shape[0] != D or down.shape[1] * 4 != F
+            or (gated and tuple(gate.shape) != tuple(up.shape))):
+        raise ValueError("FFN weight shapes do not match X")
+    _need_gain(g_in, D, "g_in")
+    _need_gain(g_sub, F, "g_sub")
+    Y = out if out is not None else torch.empty((M, D), dtype=torch.float32, device=X.device)
+    ws = _workspace(workspace, workspace_bytes(BL_OP_FFN_GATED if gated else BL_OP_FFN, M, F, D))
+    check(_lib.lib().bitlinear_ffn_subln(_ptr(X), _x_dtype(X), M, D, _ptr(g_in), _ptr(up), _ptr(s_up), _ptr(gate),
+                                         _ptr(s_gate), _ptr(g_sub), _ptr(down), _ptr(s_down), F, eps_norm, eps,
+                                         _ptr(Y), _ptr(ws), ws.numel(), _stream(stream)), "bitlinear_ffn_subln")
     return Y
 
 

@@ -56,6 +56,10 @@ SIGNATURES = {
     "bitlinear_forward_noalloc": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _f, _vp, _vp, _vp]),
     "bitlinear_ffn": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),
     "bitlinear_ffn_gated": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _f, _vp, _vp, _sz, _vp]),
+    "bitlinear_rmsnorm_quant": (_i, [_vp, _i, _i, _i, _vp, _f, _f, _vp, _vp, _vp]),
+    "bitlinear_forward_rmsnorm": (_i, [_vp, _i, _i, _i, _vp, _f, _vp, _vp, _i, _f, _vp, _vp, _vp, _sz, _vp]),
+    "bitlinear_ffn_subln": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _f, _f, _vp, _vp,
+                                 _sz, _vp]),
     "bitlinear_unpack": (_i, [_vp, _i, _i, _vp, _vp]),
     "bitlinear_workspace_status": (_i, [_vp, _vp]),
 }

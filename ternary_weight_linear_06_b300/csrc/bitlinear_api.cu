@@ -10,7 +10,7 @@
 namespace bl {
 namespace {
 
-constexpr int kAbiVersion = 101;
+constexpr int kAbiVersion = 102;
 
 // Per-device capability cache: 0 unknown, 1 compute capability 10.3, -1 other.
 std::atomic<int> g_dev_ok[64];
@@ -133,6 +133,38 @@ bl_status check_linear_args(int M, int K, const uint8_t* packed, const float* s_
   return check_device();
 }
 
+// The BitLinear forward, with the RMSNorm fused into its quantization when
+// `norm` is given.
+bl_status run_forward(const void* X, int x_dtype, int M, int K, const RmsNorm* norm, const uint8_t* packed,
+                      const float* s_w, int N, float eps, float* Y, int32_t* acc, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
+  if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
+  if (M == 0 || N == 0) return BL_OK;
+  if (!X) return BL_ERR_ARG;
+  if (!aligned16(X)) return BL_ERR_ALIGN;
+  if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
+    return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const FwdLayout L = fwd_layout(M, N, K);
+  float* m = at<float>(workspace, L.m);
+  if (M >= kGemmMinTokens) {
+    // prefill: fp16 activations in the tensor-core order, then the tcgen05 GEMM
+    void* act = at<void>(workspace, L.q);
+    if (launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, norm, true, st) != cudaSuccess)
+      return BL_ERR_CUDA;
+    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false, at<int32_t>(workspace, L.accw)),
+                                 static_cast<WsHeader*>(workspace), true, st));
+  }
+  int8_t* q = at<int8_t>(workspace, L.q);
+  if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, norm, true, st) != cudaSuccess)
+    return BL_ERR_CUDA;
+  GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
+  p.q = q;
+  p.m = m;
+  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));
+}
+
 }  // namespace
 }  // namespace bl
 
@@ -196,38 +228,36 @@ bl_status bitlinear_quant_act(const void* X, int x_dtype, int M, int K, float ep
   if (!X || !q || !m) return BL_ERR_ARG;
   if (!aligned16(X) || !aligned16(q) || !aligned16(m)) return BL_ERR_ALIGN;
   if (bl_status s = check_device(); s != BL_OK) return s;
-  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, false,
+  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, false,
                                 static_cast<cudaStream_t>(stream)));
 }
 
 bl_status bitlinear_forward(const void* X, int x_dtype, int M, int K, const uint8_t* packed, const float* s_w, int N,
                             float eps, float* Y, int32_t* acc, void* workspace, size_t workspace_bytes,
                             void* stream) {
-  if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
-  if (M < 0 || !valid_nk(N, K)) return BL_ERR_SHAPE;
-  if (M == 0 || N == 0) return BL_OK;
-  if (!X) return BL_ERR_ARG;
-  if (!aligned16(X)) return BL_ERR_ALIGN;
-  if (bl_status s = check_linear_args(M, K, packed, s_w, N, Y, acc, workspace, workspace_bytes); s != BL_OK)
-    return s;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const FwdLayout L = fwd_layout(M, N, K);
-  float* m = at<float>(workspace, L.m);
-  if (M >= kGemmMinTokens) {
-    // prefill: fp16 activations in the tensor-core order, then the tcgen05 GEMM
-    void* act = at<void>(workspace, L.q);
-    if (launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, nullptr, nullptr, true, st) != cudaSuccess)
-      return BL_ERR_CUDA;
-    return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false, at<int32_t>(workspace, L.accw)),
-                                 static_cast<WsHeader*>(workspace), true, st));
-  }
-  int8_t* q = at<int8_t>(workspace, L.q);
-  if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, nullptr, nullptr, true, st) != cudaSuccess)
-    return BL_ERR_CUDA;
-  GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
-  p.q = q;
-  p.m = m;
-  return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));
+  return run_forward(X, x_dtype, M, K, nullptr, packed, s_w, N, eps, Y, acc, workspace, workspace_bytes, stream);
+}
+
+bl_status bitlinear_rmsnorm_quant(const void* X, int x_dtype, int M, int K, const float* g, float eps_norm, float eps,
+                                  int8_t* q, float* m, void* stream) {
+  if (!valid_dtype(x_dtype) || !valid_eps(eps) || !valid_eps(eps_norm)) return BL_ERR_ARG;
+  if (M < 0 || !valid_k(K)) return BL_ERR_SHAPE;
+  if (M == 0) return BL_OK;
+  if (!X || !q || !m) return BL_ERR_ARG;
+  if (!aligned16(X) || !aligned16(q) || !aligned16(m) || (g && !aligned16(g))) return BL_ERR_ALIGN;
+  if (bl_status s = check_device(); s != BL_OK) return s;
+  const RmsNorm norm{g, eps_norm};
+  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, &norm, false,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+bl_status bitlinear_forward_rmsnorm(const void* X, int x_dtype, int M, int K, const float* g, float eps_norm,
+                                    const uint8_t* packed, const float* s_w, int N, float eps, float* Y,
+                                    int32_t* acc, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_eps(eps_norm)) return BL_ERR_ARG;
+  if (g && !aligned16(g)) return BL_ERR_ALIGN;
+  const RmsNorm norm{g, eps_norm};
+  return run_forward(X, x_dtype, M, K, &norm, packed, s_w, N, eps, Y, acc, workspace, workspace_bytes, stream);
 }
 
 bl_status bitlinear_forward_batch(const bl_forward_desc* descs, int count, float eps, void* workspace,
@@ -316,7 +346,7 @@ bl_status bitlinear_quant_act_tc(const void* X, int x_dtype, int M, int K, float
   if (!X || !act || !m) return BL_ERR_ARG;
   if (!aligned16(X) || !aligned16(act) || (reinterpret_cast<uintptr_t>(m) & 3u)) return BL_ERR_ALIGN;
   if (bl_status s = check_device(); s != BL_OK) return s;
-  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, nullptr, nullptr, false,
+  return from_cuda(launch_quant(X, x_dtype, M, K, eps, QLayout::kPairF16, act, m, nullptr, false,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -345,9 +375,12 @@ namespace {
 
 // The FFN block: up (and gate) on one quantization of X, ReLU^2 (times the up
 // projection when gated), requantization, down. gate == nullptr: ungated.
+// With n_in / n_sub the RMSNorms of SubLN are fused into the quantization of
+// X and of h.
 bl_status run_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, const float* s_up,
                   const uint8_t* gate, const float* s_gate, const uint8_t* down, const float* s_down, int F,
-                  float eps, float* Y, void* workspace, size_t workspace_bytes, void* stream) {
+                  float eps, float* Y, void* workspace, size_t workspace_bytes, void* stream,
+                  const RmsNorm* n_in = nullptr, const RmsNorm* n_sub = nullptr) {
   const bool gated = gate != nullptr || s_gate != nullptr;
   if (!valid_dtype(x_dtype) || !valid_eps(eps)) return BL_ERR_ARG;
   if (M < 0 || !valid_nk(F, D) || !valid_nk(D, F) || F == 0) return BL_ERR_SHAPE;
@@ -372,7 +405,7 @@ bl_status run_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, c
     void* ax = at<void>(workspace, L.qx);
     void* ah = at<void>(workspace, L.qh);
     int32_t* accw = at<int32_t>(workspace, L.accw);
-    if (launch_quant(X, x_dtype, M, D, eps, QLayout::kPairF16, ax, mx, nullptr, nullptr, true, st) != cudaSuccess)
+    if (launch_quant(X, x_dtype, M, D, eps, QLayout::kPairF16, ax, mx, n_in, true, st) != cudaSuccess)
       return BL_ERR_CUDA;
     if (gated) {
       if (launch_gemm(make_gemm(M, D, gate, s_gate, F, ax, mx, g, nullptr, true, accw), hdr, true, st) !=
@@ -385,14 +418,14 @@ bl_status run_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, c
                cudaSuccess) {
       return BL_ERR_CUDA;
     }
-    if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kPairF16, ah, mh, nullptr, nullptr, true, st) !=
+    if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kPairF16, ah, mh, n_sub, true, st) !=
         cudaSuccess)
       return BL_ERR_CUDA;
     return from_cuda(launch_gemm(make_gemm(M, F, down, s_down, D, ah, mh, Y, nullptr, false, accw), hdr, true, st));
   }
   int8_t* qx = at<int8_t>(workspace, L.qx);
   int8_t* qh = at<int8_t>(workspace, L.qh);
-  if (launch_quant(X, x_dtype, M, D, eps, QLayout::kRowMajorI8, qx, mx, nullptr, nullptr, true, st) != cudaSuccess)
+  if (launch_quant(X, x_dtype, M, D, eps, QLayout::kRowMajorI8, qx, mx, n_in, true, st) != cudaSuccess)
     return BL_ERR_CUDA;
   if (gated) {
     GemvProblem pg = make_problem(M, D, gate, s_gate, F, g, nullptr);
@@ -407,7 +440,7 @@ bl_status run_ffn(const void* X, int x_dtype, int M, int D, const uint8_t* up, c
   if (gated) pu.mul = g;
   else pu.epi = Epi::kRelu2;
   if (launch_gemv(pu, hdr, true, st) != cudaSuccess) return BL_ERR_CUDA;
-  if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kRowMajorI8, qh, mh, nullptr, nullptr, true, st) !=
+  if (launch_quant(h, BL_DTYPE_F32, M, F, eps, QLayout::kRowMajorI8, qh, mh, n_sub, true, st) !=
       cudaSuccess)
     return BL_ERR_CUDA;
   GemvProblem pd = make_problem(M, F, down, s_down, D, Y, nullptr);
@@ -433,6 +466,17 @@ bl_status bitlinear_ffn_gated(const void* X, int x_dtype, int M, int D, const ui
   if (!gate || !s_gate) return BL_ERR_ARG;
   return run_ffn(X, x_dtype, M, D, up, s_up, gate, s_gate, down, s_down, F, eps, Y, workspace, workspace_bytes,
                  stream);
+}
+
+bl_status bitlinear_ffn_subln(const void* X, int x_dtype, int M, int D, const float* g_in, const uint8_t* up,
+                              const float* s_up, const uint8_t* gate, const float* s_gate, const float* g_sub,
+                              const uint8_t* down, const float* s_down, int F, float eps_norm, float eps, float* Y,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!valid_eps(eps_norm) || (gate == nullptr) != (s_gate == nullptr)) return BL_ERR_ARG;
+  if ((g_in && !aligned16(g_in)) || (g_sub && !aligned16(g_sub))) return BL_ERR_ALIGN;
+  const RmsNorm n_in{g_in, eps_norm}, n_sub{g_sub, eps_norm};
+  return run_ffn(X, x_dtype, M, D, up, s_up, gate, s_gate, down, s_down, F, eps, Y, workspace, workspace_bytes,
+                 stream, &n_in, &n_sub);
 }
 
 bl_status bitlinear_unpack(const uint8_t* packed, int N, int K, int8_t* t, void* stream) {

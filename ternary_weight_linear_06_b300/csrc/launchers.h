@@ -22,12 +22,15 @@ enum class QLayout : int {
   kRowMajorI8 = 0,   // q[m][k] int8 (public layout, read by the GEMV)
   kPairF16 = 2,      // per 16 columns: fp16 slot s holds column (s>>1) + 8*(s&1) (MMA order)
 };
-// X: [M][K] fp32 or bf16. m_out [M] fp32, qsum_out [M] int32 (may be null).
-// absmax_in: when non-null, per-row absmax is taken from it instead of
-// scanning X (the FFN requant after a fused reduction).
+// RMSNorm fused into the quantization: codes from u = fp32(x * g) (g null:
+// unit gain), scale fp32(max(max|u|, eps) * r), r = 1/sqrt(mean x^2 + eps_norm).
+struct RmsNorm {
+  const float* g;        // [K] fp32 gain, or null
+  float eps_norm;        // > 0
+};
+// X: [M][K] fp32 or bf16; m_out [M] fp32; norm: null for the plain quantization.
 cudaError_t launch_quant(const void* X, int x_dtype, int M, int K, float eps, QLayout layout,
-                         void* q, float* m_out, int32_t* qsum_out, const float* absmax_in,
-                         bool pdl, cudaStream_t st);
+                         void* q, float* m_out, const RmsNorm* norm, bool pdl, cudaStream_t st);
 
 // Row-major int8 quantization of several problems in one launch.
 struct QuantProblem {

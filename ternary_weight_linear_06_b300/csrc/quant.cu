@@ -5,12 +5,20 @@
 // the 2B4T report (section 2) applies absmax per token. With Qb = 127:
 //   m = max(max_k |x_k|, eps);  q_k = clamp(rint(fp32(fp32(x_k * 127) / m)), -128, 127).
 //
-// One CTA per token row: pass 1 reduces |x| to the row absmax (skipped when
-// the caller supplies it), pass 2 quantizes 16 columns per thread step and
-// writes them in the layout the consumer wants (row-major int8, or fp16 in
-// the tensor-core operand order), plus sum_k q_k when asked. A batched
-// variant quantizes the token rows of up to kQuantMaxBatch problems in one
-// launch.
+// One CTA per token row: pass 1 reduces |x| to the row absmax, pass 2
+// quantizes 16 columns per thread step and writes them in the layout the
+// consumer wants (row-major int8, or fp16 in the tensor-core operand order).
+// Rows up to 16384 columns stay in registers between the passes.
+// A batched variant quantizes the token rows of up to kQuantMaxBatch
+// problems in one launch.
+//
+// SubLN ("BitNet b1.58 2B4T Technical Report", section 2: a sub-layer norm,
+// bias-free norm layers; RMSNorm as the LLaMA-style norm in "BitNet解读",
+// 模型架构 / 组件兼容性) runs in the same two passes: RMSNorm with gain g is
+// n = x * g * r per token, r = 1 / sqrt(mean x^2 + eps_norm). Absmax codes
+// are unchanged by the positive factor r, so pass 2 quantizes u = fp32(x * g)
+// and r goes into the token's scale; pass 1 adds the sum of x^2 to the absmax
+// reduction.
 #include "common.cuh"
 #include "launchers.h"
 
@@ -19,87 +27,210 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Quantize one token row (all threads of the CTA take part).
-template <int DT, int LAYOUT>
-__device__ __forceinline__ void quant_row(const void* __restrict__ xr, int K, float eps, void* __restrict__ qout_row,
-                                          float* __restrict__ m_out, int32_t* __restrict__ qsum_out,
-                                          const float* __restrict__ absmax_in, float* s_red, int* s_sum) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = K >> 4;
-  float amax;
-  if (absmax_in != nullptr) {
-    amax = *absmax_in;
-  } else {
-    float a = 0.0f;
-    for (int g = tid; g < G; g += kThreads) {
-      float v[16];
-      load16<DT>(xr, g, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
-    }
-    a = warp_max(a);
-    if (lane == 0) s_red[warp] = a;
-    __syncthreads();
-    a = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[w]);
-    amax = a;
-  }
-  const float m = fmaxf(amax, eps);
+// Sum of the squares of one row, carried as the unevaluated pair p + s of the
+// compensated dot product Dot2 of Ogita, Rump and Oishi ("Accurate Sum and
+// Dot Product", SIAM J. Sci. Comput. 26(6), 2005): each square is split
+// exactly into its rounded value and the FMA remainder, each addition into its
+// rounded sum and the TwoSum error. The pair holds the sum to about twice
+// fp32's precision without the fp64 pipe, which is slow on this GPU. With
+// EXACT_SQ (bf16 inputs: an 8-bit significand squares exactly in fp32) the
+// FMA remainder is known to be zero and skipped.
+struct F2 {
+  float hi, lo;
+};
 
-  int qs = 0;
-  for (int g = tid; g < G; g += kThreads) {
-    float v[16];
-    load16<DT>(xr, g, v);
-    int q[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      q[j] = quant_one(v[j], m);
-      qs += q[j];
-    }
-    if constexpr (LAYOUT == static_cast<int>(QLayout::kRowMajorI8)) {
-      uint4 o = make_uint4(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]),
-                           pack4(q[8], q[9], q[10], q[11]), pack4(q[12], q[13], q[14], q[15]));
-      reinterpret_cast<uint4*>(qout_row)[g] = o;
-    } else {
-      // fp16 slot s holds column (s >> 1) + 8 * (s & 1)
-      uint4 o0 = make_uint4(pack_h2(q[0], q[8]), pack_h2(q[1], q[9]), pack_h2(q[2], q[10]), pack_h2(q[3], q[11]));
-      uint4 o1 = make_uint4(pack_h2(q[4], q[12]), pack_h2(q[5], q[13]), pack_h2(q[6], q[14]), pack_h2(q[7], q[15]));
-      uint4* dst = reinterpret_cast<uint4*>(qout_row) + 2 * g;
-      dst[0] = o0;
-      dst[1] = o1;
-    }
-  }
-  if (qsum_out != nullptr) {
-    qs = warp_sum(qs);
-    if (lane == 0) s_sum[warp] = qs;
-    __syncthreads();
-    if (tid == 0) {
-      int t = 0;
-#pragma unroll
-      for (int w = 0; w < kThreads / 32; ++w) t += s_sum[w];
-      *qsum_out = t;
-    }
-  }
-  if (tid == 0 && m_out != nullptr) *m_out = m;
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+  const float t = __fadd_rn(a, b);
+  const float z = __fsub_rn(t, a);
+  return {t, __fadd_rn(__fsub_rn(a, __fsub_rn(t, z)), __fsub_rn(b, z))};
 }
 
-template <int DT, int LAYOUT>
+// (a.hi + a.lo) + (b.hi + b.lo) as a normalized pair; the terms here are all
+// non-negative, so nothing cancels and the error stays near 2^-44 relative.
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const F2 s = two_sum(a.hi, b.hi);
+  const float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  const float hi = __fadd_rn(s.hi, e);
+  return {hi, __fsub_rn(e, __fsub_rn(hi, s.hi))};
+}
+
+template <bool EXACT_SQ>
+struct SumSq {
+  float p = 0.0f, s = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    const float h = __fmul_rn(x, x);
+    const F2 t = two_sum(p, h);
+    p = t.hi;
+    if constexpr (EXACT_SQ) s = __fadd_rn(s, t.lo);
+    else s = __fadd_rn(s, __fadd_rn(t.lo, __fmaf_rn(x, x, -h)));
+  }
+};
+
+__device__ __forceinline__ F2 warp_sum_f2(F2 v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const F2 w = {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+    v = f2_add(v, w);
+  }
+  return v;
+}
+
+// r = 1 / sqrt(S * inv_k + eps_norm) in fp64 by Newton's iteration for the
+// inverse square root, y <- y * (3/2 - a y^2 / 2), from the fp32 estimate
+// rsqrtf(a): each step squares the relative error (about 2^-22 -> 2^-44 ->
+// below fp64 rounding), using only multiplies and FMAs.
+__device__ __forceinline__ double rms_factor(F2 S, double inv_k, float eps_norm) {
+  const double s = __dadd_rn(static_cast<double>(S.hi), static_cast<double>(S.lo));
+  const double a = __fma_rn(s, inv_k, static_cast<double>(eps_norm));
+  double y = static_cast<double>(rsqrtf(__double2float_rn(a)));
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const double t = __dmul_rn(__dmul_rn(a, y), y);
+    y = __dmul_rn(y, __fma_rn(-0.5, t, 1.5));
+  }
+  return y;
+}
+
+// u = fp32(x * g) for the 16 columns of group g (x stays as it is without a gain).
+__device__ __forceinline__ void apply_gain(const float* __restrict__ gain, int g, float (&v)[16]) {
+  if (gain == nullptr) return;
+  float w[16];
+  load16<BL_DTYPE_F32>(gain, g, w);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], w[j]);
+}
+
+// Pass-1 work on one 16-column group: with NORM, the squares of x go into the
+// two sum chains and v becomes u = fp32(x * g); then the running absmax.
+template <int DT, bool NORM>
+__device__ __forceinline__ void stat_group(float (&v)[16], int g, const float* __restrict__ gain,
+                                           SumSq<DT == BL_DTYPE_BF16>& ss0, SumSq<DT == BL_DTYPE_BF16>& ss1,
+                                           float& a) {
+  if constexpr (NORM) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      ss0.add(v[j]);
+      ss1.add(v[j + 1]);
+    }
+    apply_gain(gain, g, v);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
+}
+
+// Pass-2 work on one group: the codes, written in the consumer's layout.
+template <int LAYOUT>
+__device__ __forceinline__ void store_group(const float (&v)[16], int g, float m, float rm,
+                                            void* __restrict__ qout_row) {
+  int q[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) q[j] = quant_code(v[j], m, rm);
+  if constexpr (LAYOUT == static_cast<int>(QLayout::kRowMajorI8)) {
+    uint4 o = make_uint4(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]),
+                         pack4(q[8], q[9], q[10], q[11]), pack4(q[12], q[13], q[14], q[15]));
+    reinterpret_cast<uint4*>(qout_row)[g] = o;
+  } else {
+    // fp16 slot s holds column (s >> 1) + 8 * (s & 1)
+    uint4 o0 = make_uint4(pack_h2(q[0], q[8]), pack_h2(q[1], q[9]), pack_h2(q[2], q[10]), pack_h2(q[3], q[11]));
+    uint4 o1 = make_uint4(pack_h2(q[4], q[12]), pack_h2(q[5], q[13]), pack_h2(q[6], q[14]), pack_h2(q[7], q[15]));
+    uint4* dst = reinterpret_cast<uint4*>(qout_row) + 2 * g;
+    dst[0] = o0;
+    dst[1] = o1;
+  }
+}
+
+// Groups of 16 columns each thread keeps in registers between the passes (0:
+// the row is too long, pass 2 reads it again).
+constexpr int kMaxResident = 4;
+inline int resident_groups(int K) {
+  const int G = K >> 4;
+  if (G <= kThreads) return 1;
+  if (G <= 2 * kThreads) return 2;
+  if (G <= kMaxResident * kThreads) return 4;
+  return 0;
+}
+
+// Quantize one token row (all threads of the CTA take part). With NORM the
+// row is first RMS-normalized with the gain `gain` (null: unit gain): codes
+// come from u = fp32(x * g) and the scale written is
+// fp32(max(max|u|, eps) * r), r = 1 / sqrt(sum x^2 / K + eps_norm); inv_k = 1/K.
+// R > 0: thread t holds groups t + i * kThreads (i < R) in registers, loaded
+// once; R = 0: both passes stream the row.
+template <int DT, int LAYOUT, bool NORM, int R>
+__device__ __forceinline__ void quant_row(const void* __restrict__ xr, int K, float eps,
+                                          const float* __restrict__ gain, float eps_norm, double inv_k,
+                                          void* __restrict__ qout_row, float* __restrict__ m_out, float* s_red,
+                                          F2* s_ss) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = K >> 4;
+  float a = 0.0f;
+  SumSq<DT == BL_DTYPE_BF16> ss0, ss1;        // two chains (even, odd columns) for latency
+  float v[R > 0 ? R : 1][16];
+  if constexpr (R > 0) {
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (tid + i * kThreads < G) load16<DT>(xr, tid + i * kThreads, v[i]);
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (tid + i * kThreads < G) stat_group<DT, NORM>(v[i], tid + i * kThreads, gain, ss0, ss1, a);
+  } else {
+    for (int g = tid; g < G; g += kThreads) {
+      load16<DT>(xr, g, v[0]);
+      stat_group<DT, NORM>(v[0], g, gain, ss0, ss1, a);
+    }
+  }
+  a = warp_max(a);
+  if (lane == 0) s_red[warp] = a;
+  if constexpr (NORM) {
+    const F2 d = warp_sum_f2(f2_add({ss0.p, ss0.s}, {ss1.p, ss1.s}));
+    if (lane == 0) s_ss[warp] = d;
+  }
+  __syncthreads();
+  a = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[w]);
+  const float m = fmaxf(a, eps);
+  const float rm = __frcp_rn(m);
+
+  if constexpr (R > 0) {
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (tid + i * kThreads < G) store_group<LAYOUT>(v[i], tid + i * kThreads, m, rm, qout_row);
+  } else {
+    for (int g = tid; g < G; g += kThreads) {
+      load16<DT>(xr, g, v[0]);
+      if constexpr (NORM) apply_gain(gain, g, v[0]);
+      store_group<LAYOUT>(v[0], g, m, rm, qout_row);
+    }
+  }
+  if (tid == 0 && m_out != nullptr) {
+    if constexpr (NORM) {
+      F2 S = s_ss[0];
+#pragma unroll
+      for (int w = 1; w < kThreads / 32; ++w) S = f2_add(S, s_ss[w]);
+      const double r = rms_factor(S, inv_k, eps_norm);
+      *m_out = __double2float_rn(__dmul_rn(static_cast<double>(m), r));
+    } else {
+      *m_out = m;
+    }
+  }
+}
+
+template <int DT, int LAYOUT, bool NORM, int R>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict__ X, int K, float eps,
-                                                         void* __restrict__ qout, float* __restrict__ m_out,
-                                                         int32_t* __restrict__ qsum_out,
-                                                         const float* __restrict__ absmax_in) {
+                                                         const float* __restrict__ gain, float eps_norm,
+                                                         double inv_k, void* __restrict__ qout,
+                                                         float* __restrict__ m_out) {
   __shared__ float s_red[kThreads / 32];
-  __shared__ int s_sum[kThreads / 32];
+  __shared__ F2 s_ss[kThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int row = blockIdx.x;
   const size_t esize = DT == BL_DTYPE_F32 ? 4 : 2;
   const size_t qsize = LAYOUT == static_cast<int>(QLayout::kRowMajorI8) ? 1 : 2;
-  quant_row<DT, LAYOUT>(static_cast<const char*>(X) + static_cast<size_t>(row) * K * esize, K, eps,
-                        static_cast<char*>(qout) + static_cast<size_t>(row) * K * qsize,
-                        m_out != nullptr ? m_out + row : nullptr, qsum_out != nullptr ? qsum_out + row : nullptr,
-                        absmax_in != nullptr ? absmax_in + row : nullptr, s_red, s_sum);
+  quant_row<DT, LAYOUT, NORM, R>(static_cast<const char*>(X) + static_cast<size_t>(row) * K * esize, K, eps, gain,
+                                 eps_norm, inv_k, static_cast<char*>(qout) + static_cast<size_t>(row) * K * qsize,
+                                 m_out + row, s_red, s_ss);
 }
 
 // Row-major int8 quantization of the token rows of several problems in one
@@ -111,9 +242,9 @@ struct QuantBatchArgs {
   float eps;
 };
 
+template <int R>
 __global__ void __launch_bounds__(kThreads) quant_batch_kernel(const __grid_constant__ QuantBatchArgs a) {
   __shared__ float s_red[kThreads / 32];
-  __shared__ int s_sum[kThreads / 32];
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -129,14 +260,14 @@ __global__ void __launch_bounds__(kThreads) quant_batch_kernel(const __grid_cons
   const void* xr = static_cast<const char*>(P.X) + static_cast<size_t>(row) * P.K * esize;
   int8_t* qr = P.q + static_cast<size_t>(row) * P.K;
   if (P.x_dtype == BL_DTYPE_F32)
-    quant_row<BL_DTYPE_F32, 0>(xr, P.K, a.eps, qr, P.m + row, nullptr, nullptr, s_red, s_sum);
+    quant_row<BL_DTYPE_F32, 0, false, R>(xr, P.K, a.eps, nullptr, 0.0f, 0.0, qr, P.m + row, s_red, nullptr);
   else
-    quant_row<BL_DTYPE_BF16, 0>(xr, P.K, a.eps, qr, P.m + row, nullptr, nullptr, s_red, s_sum);
+    quant_row<BL_DTYPE_BF16, 0, false, R>(xr, P.K, a.eps, nullptr, 0.0f, 0.0, qr, P.m + row, s_red, nullptr);
 }
 
-template <int DT, int LAYOUT>
-cudaError_t launch_t(const void* X, int M, int K, float eps, void* q, float* m_out, int32_t* qsum_out,
-                     const float* absmax_in, bool pdl, cudaStream_t st) {
+template <int DT, int LAYOUT, bool NORM, int R>
+cudaError_t launch_t(const void* X, int M, int K, float eps, const RmsNorm* norm, void* q, float* m_out, bool pdl,
+                     cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
   cfg.stream = st;
@@ -146,7 +277,26 @@ cudaError_t launch_t(const void* X, int M, int K, float eps, void* q, float* m_o
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cfg.gridDim = dim3(static_cast<unsigned>(M));
-  return cudaLaunchKernelEx(&cfg, quant_kernel<DT, LAYOUT>, X, K, eps, q, m_out, qsum_out, absmax_in);
+  return cudaLaunchKernelEx(&cfg, quant_kernel<DT, LAYOUT, NORM, R>, X, K, eps, NORM ? norm->g : nullptr,
+                            NORM ? norm->eps_norm : 0.0f, 1.0 / static_cast<double>(K), q, m_out);
+}
+
+template <int DT, int LAYOUT, bool NORM>
+cudaError_t launch_r(const void* X, int M, int K, float eps, const RmsNorm* norm, void* q, float* m_out, bool pdl,
+                     cudaStream_t st) {
+  switch (resident_groups(K)) {
+    case 1: return launch_t<DT, LAYOUT, NORM, 1>(X, M, K, eps, norm, q, m_out, pdl, st);
+    case 2: return launch_t<DT, LAYOUT, NORM, 2>(X, M, K, eps, norm, q, m_out, pdl, st);
+    case 4: return launch_t<DT, LAYOUT, NORM, 4>(X, M, K, eps, norm, q, m_out, pdl, st);
+    default: return launch_t<DT, LAYOUT, NORM, 0>(X, M, K, eps, norm, q, m_out, pdl, st);
+  }
+}
+
+template <int DT, int LAYOUT>
+cudaError_t launch_n(const void* X, int M, int K, float eps, const RmsNorm* norm, void* q, float* m_out, bool pdl,
+                     cudaStream_t st) {
+  if (norm != nullptr) return launch_r<DT, LAYOUT, true>(X, M, K, eps, norm, q, m_out, pdl, st);
+  return launch_r<DT, LAYOUT, false>(X, M, K, eps, norm, q, m_out, pdl, st);
 }
 
 // int8 row-major -> fp16 in the tensor-core pair order (an input quantized
@@ -210,19 +360,26 @@ cudaError_t launch_quant_batch(const QuantProblem* ps, int count, float eps, boo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, quant_batch_kernel, a);
+  int max_k = 0;
+  for (int i = 0; i < n; ++i) max_k = std::max(max_k, a.prob[i].K);
+  switch (resident_groups(max_k)) {
+    case 1: return cudaLaunchKernelEx(&cfg, quant_batch_kernel<1>, a);
+    case 2: return cudaLaunchKernelEx(&cfg, quant_batch_kernel<2>, a);
+    case 4: return cudaLaunchKernelEx(&cfg, quant_batch_kernel<4>, a);
+    default: return cudaLaunchKernelEx(&cfg, quant_batch_kernel<0>, a);
+  }
 }
 
 cudaError_t launch_quant(const void* X, int x_dtype, int M, int K, float eps, QLayout layout, void* q,
-                         float* m_out, int32_t* qsum_out, const float* absmax_in, bool pdl, cudaStream_t st) {
+                         float* m_out, const RmsNorm* norm, bool pdl, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  const int L = static_cast<int>(layout);
+  const bool i8 = layout == QLayout::kRowMajorI8;
   if (x_dtype == BL_DTYPE_F32) {
-    if (L == 0) return launch_t<BL_DTYPE_F32, 0>(X, M, K, eps, q, m_out, qsum_out, absmax_in, pdl, st);
-    return launch_t<BL_DTYPE_F32, 2>(X, M, K, eps, q, m_out, qsum_out, absmax_in, pdl, st);
+    if (i8) return launch_n<BL_DTYPE_F32, 0>(X, M, K, eps, norm, q, m_out, pdl, st);
+    return launch_n<BL_DTYPE_F32, 2>(X, M, K, eps, norm, q, m_out, pdl, st);
   }
-  if (L == 0) return launch_t<BL_DTYPE_BF16, 0>(X, M, K, eps, q, m_out, qsum_out, absmax_in, pdl, st);
-  return launch_t<BL_DTYPE_BF16, 2>(X, M, K, eps, q, m_out, qsum_out, absmax_in, pdl, st);
+  if (i8) return launch_n<BL_DTYPE_BF16, 0>(X, M, K, eps, norm, q, m_out, pdl, st);
+  return launch_n<BL_DTYPE_BF16, 2>(X, M, K, eps, norm, q, m_out, pdl, st);
 }
 
 }  // namespace bl

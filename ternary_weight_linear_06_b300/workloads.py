@@ -114,3 +114,16 @@ def large_weights(shape: str) -> np.ndarray:
     K, N = SHAPES_70B[shape]
     off = {"attn": 0, "up": 1, "down": 2}[shape]
     return gaussian_weights(N, K, 0.01, 7000 + off, outlier_frac=0.001)
+
+
+def norm_gain(K: int, seed: int, edge: bool = True) -> np.ndarray:
+    """RMSNorm gain [K] ~ U(0.05, 2.5), fp32 (norm gains are mostly positive
+    and of order one). With ``edge``, 1% of the entries are negated and 0.5%
+    set to zero, so that signs and dropped columns are exercised."""
+    rng = np.random.default_rng(seed)
+    g = rng.uniform(0.05, 2.5, K).astype(np.float32)
+    if edge:
+        neg = rng.choice(K, size=max(1, K // 100), replace=False)
+        g[neg] = -g[neg]
+        g[rng.choice(K, size=max(1, K // 200), replace=False)] = 0.0
+    return g

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     lib = _lib.lib()
-    assert lib.bitlinear_version() == 101
+    assert lib.bitlinear_version() == 102
     for s in range(8):
         assert lib.bitlinear_status_str(s)
     assert b"unknown" in lib.bitlinear_status_str(99)
@@ -81,6 +81,34 @@ def test_host_argument_checks_fail_before_launch():
     assert lib.bitlinear_ffn_gated(p, 0, 2, 64, p, p, p, p, p, p, 128, 1e-5, p, p, need - 256, None) == \
         _lib.BL_ERR_WORKSPACE
     assert lib.bitlinear_ffn_gated(p, 0, 2, 64, p, p, p + 4, p, p, p, 128, 1e-5, p, p, need, None) == _lib.BL_ERR_ALIGN
+    # RMSNorm fused into the quantization: eps_norm must be positive and finite,
+    # the gain 16-byte aligned (or NULL)
+    nan = float("nan")
+    assert lib.bitlinear_rmsnorm_quant(p, 0, 2, 64, p, 0.0, 1e-5, p, p, None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_rmsnorm_quant(p, 0, 2, 64, p, nan, 1e-5, p, p, None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_rmsnorm_quant(p, 0, 2, 96, p, 1e-5, 1e-5, p, p, None) == _lib.BL_ERR_SHAPE
+    assert lib.bitlinear_rmsnorm_quant(p, 0, 2, 64, p + 4, 1e-5, 1e-5, p, p, None) == _lib.BL_ERR_ALIGN
+    assert lib.bitlinear_rmsnorm_quant(None, 0, 0, 64, None, 1e-5, 1e-5, None, None, None) == _lib.BL_OK
+    assert lib.bitlinear_forward_rmsnorm(p, 0, 1, 64, p, -1.0, p, p, 4, 1e-5, p, None, p, 4096, None) == \
+        _lib.BL_ERR_ARG
+    assert lib.bitlinear_forward_rmsnorm(p, 0, 1, 64, p + 8, 1e-5, p, p, 4, 1e-5, p, None, p, 4096, None) == \
+        _lib.BL_ERR_ALIGN
+    assert lib.bitlinear_forward_rmsnorm(p, 0, 1, 64, None, 1e-5, p, p, 4, 1e-5, p, None, p, 16, None) == \
+        _lib.BL_ERR_WORKSPACE
+    assert lib.bitlinear_forward_rmsnorm(p, 0, 1, 96, None, 1e-5, p, p, 4, 1e-5, p, None, p, 4096, None) == \
+        _lib.BL_ERR_SHAPE
+    assert lib.bitlinear_forward_rmsnorm(None, 0, 0, 64, None, 1e-5, None, None, 4, 1e-5, None, None, None, 0,
+                                         None) == _lib.BL_OK
+    # SubLN FFN: gate and s_gate together; the gated form needs the gated workspace
+    assert lib.bitlinear_ffn_subln(p, 0, 2, 64, None, p, p, p, None, None, p, p, 128, 1e-5, 1e-5, p, p, 1 << 20,
+                                   None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_ffn_subln(p, 0, 2, 64, None, p, p, None, None, None, p, p, 128, 0.0, 1e-5, p, p, 1 << 20,
+                                   None) == _lib.BL_ERR_ARG
+    assert lib.bitlinear_ffn_subln(p, 0, 2, 64, None, p, p, None, None, p + 4, p, p, 128, 1e-5, 1e-5, p, p,
+                                   1 << 20, None) == _lib.BL_ERR_ALIGN
+    plain = lib.bitlinear_workspace_bytes(_lib.BL_OP_FFN, 2, 128, 64)
+    assert lib.bitlinear_ffn_subln(p, 0, 2, 64, None, p, p, p, p, None, p, p, 128, 1e-5, 1e-5, p, p, plain,
+                                   None) == _lib.BL_ERR_WORKSPACE
     # tensor-core operand form
     assert lib.bitlinear_quant_act_tc(p, 0, 2, 96, 1e-5, p, p, None) == _lib.BL_ERR_SHAPE
     assert lib.bitlinear_quant_act_tc(p, 0, 2, 64, 1e-5, p + 8, p, None) == _lib.BL_ERR_ALIGN

@@ -500,3 +500,146 @@ def test_gated_ffn_2b_shapes_split_k():
     Y = BL.ffn_gated(dev(X), up, s_up, gate, s_gate, down, s_down)
     Y_ref, _ = O.ffn_gated(X, tu, su, tg, sg, td, sd)
     assert_y(host(Y), Y_ref)
+
+
+# ----------------------------------------------------------------- SubLN RMSNorm fused into the quantization
+# Codes and accumulators are bit-exact. The norm factor comes from a
+# compensated fp32 sum of squares on the GPU and from the exact sum in the
+# oracle, so a token scale m may sit one fp32 step off where the exact value
+# is that close to a rounding boundary; where m agrees, Y agrees bit for bit.
+def assert_m_close(m_gpu, m_ref):
+    a = np.asarray(m_gpu, np.float32).view(np.int32).astype(np.int64)
+    b = np.asarray(m_ref, np.float32).view(np.int32).astype(np.int64)
+    assert np.all(a > 0) and np.all(b > 0)
+    d = np.abs(a - b)
+    assert d.max(initial=0) <= 1, d.max()
+    return d == 0
+
+
+def assert_y_norm(Y_gpu, Y_ref, m_same):
+    Y_gpu = np.asarray(Y_gpu, np.float32)
+    Y_ref = np.asarray(Y_ref, np.float32)
+    rel = np.abs(Y_gpu.astype(np.float64) - Y_ref) / np.maximum(np.abs(Y_ref.astype(np.float64)), 1e-30)
+    assert rel.max(initial=0.0) <= RTOL, rel.max()
+    np.testing.assert_array_equal(Y_gpu[m_same].view(np.uint32), Y_ref[m_same].view(np.uint32))
+
+
+def _norm_rows(M, K, seed, dtype):
+    X = WL.prefill_activations(M, K, seed=seed)
+    if M >= 4:
+        X[1] = 0.0                                   # all-zero token: codes 0, scale eps * r
+        X[2] *= np.float32(1e-20)                    # far below eps_norm
+        X[3] = np.float32(-3.5)                      # constant token
+    if M >= 5:
+        X[4] *= np.float32(1e15)                     # sum of squares near 1e34, still finite in fp32
+    if dtype == "bf16":
+        bits = WL.f32_to_bf16_bits(X)
+        return bits, O.bf16_bits_to_f32(bits)
+    return X, X
+
+
+@pytest.mark.parametrize("M,K,dtype,gain", [
+    (1, 2560, "f32", True), (3, 64, "bf16", False), (6, 6912, "f32", True), (64, 2560, "bf16", True),
+    (257, 320, "f32", True), (2, 65536, "f32", True), (5, 65536, "bf16", False)])
+def test_rmsnorm_quant_matches_oracle(M, K, dtype, gain):
+    X_in, X32 = _norm_rows(M, K, 300 + M, dtype)
+    g = WL.norm_gain(K, seed=310 + M) if gain else None
+    Xd = dev(X_in).view(torch.bfloat16) if dtype == "bf16" else dev(X_in)
+    q, m = BL.rmsnorm_quant(Xd, None if g is None else dev(g))
+    q_ref, m_ref = O.rmsnorm_quant(X32, g)
+    np.testing.assert_array_equal(host(q), q_ref)
+    assert_m_close(host(m), m_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2560, 2560), (4, 640, 2560), (9, 6912, 2560), (16, 2560, 6912),
+                                   (200, 1000, 320), (1000, 384, 512)])
+def test_forward_rmsnorm_all_paths(M, N, K):
+    # 1 and 4 tokens: GEMV; 9 and 16: split-K GEMM; 200 and 1000: tiled GEMM
+    W = WL.gaussian_weights(N, K, 0.02, seed=320 + M, outlier_frac=0.001)
+    X, _ = _norm_rows(M, K, 330 + M, "f32")
+    g = WL.norm_gain(K, seed=340 + M)
+    packed, s_w = BL.pack(dev(W))
+    _, s_ref, t_ref = O.pack_weights(W)
+    Y, acc = BL.forward_rmsnorm(dev(X), packed, s_w, dev(g), return_acc=True)
+    Y_ref, acc_ref, _, m_ref = O.forward_rmsnorm(X, t_ref, s_ref, g)
+    np.testing.assert_array_equal(host(acc), acc_ref)
+    _, m = BL.rmsnorm_quant(dev(X), dev(g))
+    same = assert_m_close(host(m), m_ref)
+    assert_y_norm(host(Y), Y_ref, same)
+    assert BL.workspace_status() == 0
+
+
+def test_rmsnorm_quant_feeds_the_decode_batch():
+    # one norm + quantization of a token, shared by q, k and v as prequantized
+    # batch problems, equals three forwards on RMSNorm(x)
+    K = 2560
+    X = WL.decode_activations("qo", 0, M=2)
+    g = WL.norm_gain(K, seed=350)
+    q, m = BL.rmsnorm_quant(dev(X), dev(g))
+    probs, refs = [], []
+    for i, shape in enumerate(("qo", "kv", "kv")):
+        W = WL.decode_weights(shape, 40 + i)
+        packed, s_w = BL.pack(dev(W))
+        _, s_ref, t_ref = O.pack_weights(W)
+        Y = torch.empty((2, W.shape[0]), dtype=torch.float32, device="cuda")
+        probs.append((q, packed, s_w, Y, None, m))
+        refs.append(O.forward_rmsnorm(X, t_ref, s_ref, g))
+    BL.forward_batch(probs)
+    _, m_ref = O.rmsnorm_quant(X, g)
+    same = assert_m_close(host(m), m_ref)
+    for (_, _, _, Y, _, _), (Y_ref, _, _, _) in zip(probs, refs):
+        assert_y_norm(host(Y), Y_ref, same)
+
+
+def _check_ffn_subln(Y_gpu, X, tu, su, td, sd, g_in, g_sub, tg=None, sg=None):
+    # The GPU's h equals the oracle's wherever the input scale m agrees; a
+    # scale one fp32 step off moves h by about one step, which can flip a code
+    # of h only where 127 u / m lies within 1e-4 of a half-integer. Each such
+    # code may move Y by one dequant step times |t|; nothing else may differ.
+    Y_ref, h = O.ffn_subln(X, tu, su, td, sd, g_in=g_in, g_sub=g_sub, t_gate=tg, s_gate=sg)
+    u = h if g_sub is None else (h * g_sub[None, :]).astype(np.float32)
+    m_u = np.maximum(np.abs(u).max(axis=1), O.EPS).astype(np.float32)
+    v = (u * np.float32(127)) / m_u[:, None]
+    amb = np.abs(np.abs(v - np.floor(v)) - 0.5) < 1e-4
+    _, m_h = O.rmsnorm_quant(h, g_sub)
+    step = float(sd) * m_h.astype(np.float64) / 127.0
+    slack = step[:, None] * (amb.astype(np.float64) @ np.abs(td.astype(np.float64)).T)
+    Y_gpu = np.asarray(Y_gpu, np.float32).astype(np.float64)
+    err = np.abs(Y_gpu - Y_ref.astype(np.float64))
+    assert np.all(err <= RTOL * np.abs(Y_ref.astype(np.float64)) + 1.001 * slack), (err.max(), int(amb.sum()))
+
+
+@pytest.mark.parametrize("gated", [False, True])
+@pytest.mark.parametrize("M", [1, 4, 16, 200])
+def test_ffn_subln_all_paths(M, gated):
+    D, F = 256, 640
+    Wu = WL.gaussian_weights(F, D, 0.02, seed=360 + M, outlier_frac=0.001)
+    Wg = WL.gaussian_weights(F, D, 0.02, seed=370 + M, outlier_frac=0.001)
+    Wd = WL.gaussian_weights(D, F, 0.02, seed=380 + M, outlier_frac=0.001)
+    X = WL.prefill_activations(M, D, seed=390 + M)
+    g_in, g_sub = WL.norm_gain(D, seed=400 + M), WL.norm_gain(F, seed=410 + M)
+    up, s_up = BL.pack(dev(Wu))
+    gate, s_gate = BL.pack(dev(Wg))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sg, tg = O.pack_weights(Wg)
+    _, sd, td = O.pack_weights(Wd)
+    kw = dict(gate=gate, s_gate=s_gate) if gated else {}
+    Y = BL.ffn_subln(dev(X), up, s_up, down, s_down, g_in=dev(g_in), g_sub=dev(g_sub), **kw)
+    _check_ffn_subln(host(Y), X, tu, su, td, sd, g_in, g_sub, *((tg, sg) if gated else ()))
+    assert BL.workspace_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 12])
+def test_ffn_subln_2b_shapes_unit_gains(M):
+    D, F = 2560, 6912
+    Wu, Wg, Wd = WL.decode_weights("up", 8), WL.decode_weights("up", 9), WL.decode_weights("down", 8)
+    X = WL.student_t(M, D, seed=420 + M)
+    up, s_up = BL.pack(dev(Wu))
+    gate, s_gate = BL.pack(dev(Wg))
+    down, s_down = BL.pack(dev(Wd))
+    _, su, tu = O.pack_weights(Wu)
+    _, sg, tg = O.pack_weights(Wg)
+    _, sd, td = O.pack_weights(Wd)
+    Y = BL.ffn_subln(dev(X), up, s_up, down, s_down, gate=gate, s_gate=s_gate)
+    _check_ffn_subln(host(Y), X, tu, su, td, sd, None, None, tg, sg)
