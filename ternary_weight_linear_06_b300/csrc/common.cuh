@@ -71,20 +71,26 @@ __device__ __forceinline__ float dequant_factor(float s_w, float m) {
 }
 
 // Per-token quantization of one value, clamp(rint(fp32(fp32(x*127)/m)), -128,
-// 127), without a division in almost every case; rm = fp32(1/m) and |x| <= m. With a = fp32(x*127) the quotient is c = a/m, |c| <= 127. The
-// product fp32(a*rm) carries two roundings of relative size 2^-24 each, so it
-// lies within 127 * 2^-23 < 1.6e-5 of c; fp32(c) lies within half an fp32
-// step (below 7.7e-6 for |c| < 128) of c. Both therefore round to the same
-// integer unless the product is within 2.4e-5 of a half-integer; there
-// (about one value in 10^4) the correctly rounded quotient decides.
-__device__ __forceinline__ int quant_code(float x, float m, float rm) {
-  const float a = __fmul_rn(x, 127.0f);
-  const float c = __fmul_rn(a, rm);
+// 127), for |x| <= m (m is the row's absmax or eps): returned as the integer
+// code in fp32. The clamp never binds then: |fp32(x*127)| <= fp32(127 m) <=
+// 127 m (1 + 2^-24), so the quotient rounds to at most 127 in magnitude.
+// s127 = fp32(127 * fp32(1/m)). The product c = fp32(x * s127) carries three
+// roundings of relative size 2^-24, so it lies within 127 * 3 * 2^-24 <
+// 2.3e-5 of the real 127 x / m, and the defined quotient within 1.2e-5 of it
+// (one rounding of x * 127, one of the division, each at most half an fp32
+// step of a value below 128). Both round to the same integer unless c is
+// within 3.5e-5 of a half-integer; within 1e-4 of one (about one value in
+// 5000) the defined division decides.
+__device__ __forceinline__ float quant_round(float x, float m, float s127) {
+  const float c = __fmul_rn(x, s127);
   float r = rintf(c);
-  if (fabsf(fabsf(__fsub_rn(c, r)) - 0.5f) < 6.0e-5f) r = rintf(__fdiv_rn(a, m));
-  r = fminf(fmaxf(r, -128.0f), 127.0f);
-  return __float2int_rn(r);
+  if (fabsf(__fsub_rn(c, r)) > 0.4999f) r = rintf(__fdiv_rn(__fmul_rn(x, 127.0f), m));
+  return r;
 }
+
+// Adding 1.5 * 2^23 to an integer-valued float of magnitude below 2^22 puts
+// the integer, in two's complement, in the low bits of the result.
+constexpr float kIntShift = 12582912.0f;
 
 // Load 16 consecutive activations of one row (fp32, or bf16 widened exactly).
 template <int DT>

@@ -19,6 +19,8 @@
 // are unchanged by the positive factor r, so pass 2 quantizes u = fp32(x * g)
 // and r goes into the token's scale; pass 1 adds the sum of x^2 to the absmax
 // reduction.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "launchers.h"
 
@@ -118,24 +120,36 @@ __device__ __forceinline__ void stat_group(float (&v)[16], int g, const float* _
   for (int j = 0; j < 16; ++j) a = fmaxf(a, fabsf(v[j]));
 }
 
-// Pass-2 work on one group: the codes, written in the consumer's layout.
+// Pass-2 work on one group: the codes, written in the consumer's layout
+// (s127 = fp32(127 * fp32(1/m))).
 template <int LAYOUT>
-__device__ __forceinline__ void store_group(const float (&v)[16], int g, float m, float rm,
+__device__ __forceinline__ void store_group(const float (&v)[16], int g, float m, float s127,
                                             void* __restrict__ qout_row) {
-  int q[16];
+  float r[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) q[j] = quant_code(v[j], m, rm);
+  for (int j = 0; j < 16; ++j) r[j] = quant_round(v[j], m, s127);
   if constexpr (LAYOUT == static_cast<int>(QLayout::kRowMajorI8)) {
-    uint4 o = make_uint4(pack4(q[0], q[1], q[2], q[3]), pack4(q[4], q[5], q[6], q[7]),
-                         pack4(q[8], q[9], q[10], q[11]), pack4(q[12], q[13], q[14], q[15]));
-    reinterpret_cast<uint4*>(qout_row)[g] = o;
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t b0 = __float_as_uint(__fadd_rn(r[4 * k + 0], kIntShift));
+      const uint32_t b1 = __float_as_uint(__fadd_rn(r[4 * k + 1], kIntShift));
+      const uint32_t b2 = __float_as_uint(__fadd_rn(r[4 * k + 2], kIntShift));
+      const uint32_t b3 = __float_as_uint(__fadd_rn(r[4 * k + 3], kIntShift));
+      w[k] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+    }
+    reinterpret_cast<uint4*>(qout_row)[g] = make_uint4(w[0], w[1], w[2], w[3]);
   } else {
-    // fp16 slot s holds column (s >> 1) + 8 * (s & 1)
-    uint4 o0 = make_uint4(pack_h2(q[0], q[8]), pack_h2(q[1], q[9]), pack_h2(q[2], q[10]), pack_h2(q[3], q[11]));
-    uint4 o1 = make_uint4(pack_h2(q[4], q[12]), pack_h2(q[5], q[13]), pack_h2(q[6], q[14]), pack_h2(q[7], q[15]));
+    // fp16 slot s holds column (s >> 1) + 8 * (s & 1); the codes are exact in fp16
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __half2 p2 = __floats2half2_rn(r[j], r[j + 8]);
+      h[j] = *reinterpret_cast<const uint32_t*>(&p2);
+    }
     uint4* dst = reinterpret_cast<uint4*>(qout_row) + 2 * g;
-    dst[0] = o0;
-    dst[1] = o1;
+    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
   }
 }
 
@@ -190,17 +204,17 @@ __device__ __forceinline__ void quant_row(const void* __restrict__ xr, int K, fl
 #pragma unroll
   for (int w = 0; w < kThreads / 32; ++w) a = fmaxf(a, s_red[w]);
   const float m = fmaxf(a, eps);
-  const float rm = __frcp_rn(m);
+  const float s127 = __fmul_rn(127.0f, __frcp_rn(m));
 
   if constexpr (R > 0) {
 #pragma unroll
     for (int i = 0; i < R; ++i)
-      if (tid + i * kThreads < G) store_group<LAYOUT>(v[i], tid + i * kThreads, m, rm, qout_row);
+      if (tid + i * kThreads < G) store_group<LAYOUT>(v[i], tid + i * kThreads, m, s127, qout_row);
   } else {
     for (int g = tid; g < G; g += kThreads) {
       load16<DT>(xr, g, v[0]);
       if constexpr (NORM) apply_gain(gain, g, v[0]);
-      store_group<LAYOUT>(v[0], g, m, rm, qout_row);
+      store_group<LAYOUT>(v[0], g, m, s127, qout_row);
     }
   }
   if (tid == 0 && m_out != nullptr) {
@@ -231,6 +245,169 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const void* __restrict_
   quant_row<DT, LAYOUT, NORM, R>(static_cast<const char*>(X) + static_cast<size_t>(row) * K * esize, K, eps, gain,
                                  eps_norm, inv_k, static_cast<char*>(qout) + static_cast<size_t>(row) * K * qsize,
                                  m_out + row, s_red, s_ss);
+}
+
+// ---------------------------------------------------------------------------
+// Team kernel: a row belongs to a team of TW warps (TW = 1, 2, 4 or 8, the
+// fewest for which each lane holds at most GMAX groups of 16 columns), and a
+// 256-thread CTA holds 8 / TW teams. Each lane keeps the raw input words of
+// its groups (t + 32 TW i) in registers from pass 1 to pass 2, and a team
+// meets only on its own named barrier, so an SM works on up to 64 / TW rows
+// at once rather than one per CTA.
+// ---------------------------------------------------------------------------
+template <int DT>
+constexpr int kTeamGroups = DT == BL_DTYPE_F32 ? 2 : 4;     // GMAX: 32 registers of raw input per lane
+
+template <int DT>
+struct Raw16 {
+  uint4 u[DT == BL_DTYPE_F32 ? 4 : 2];
+};
+
+template <int DT>
+__device__ __forceinline__ void load_raw(const void* row, int g, Raw16<DT>& r) {
+  const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(row) + static_cast<size_t>(g) * sizeof(Raw16<DT>));
+#pragma unroll
+  for (int i = 0; i < (DT == BL_DTYPE_F32 ? 4 : 2); ++i) r.u[i] = __ldg(p + i);
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_raw(const Raw16<DT>& r, float (&v)[16]) {
+  if constexpr (DT == BL_DTYPE_F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[4 * i + 0] = __uint_as_float(r.u[i].x);
+      v[4 * i + 1] = __uint_as_float(r.u[i].y);
+      v[4 * i + 2] = __uint_as_float(r.u[i].z);
+      v[4 * i + 3] = __uint_as_float(r.u[i].w);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t w[4] = {r.u[i].x, r.u[i].y, r.u[i].z, r.u[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * i + 2 * j + 0] = __uint_as_float(w[j] << 16);          // exact bf16 -> fp32
+        v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+// Running absmax over the raw input words of one group without widening:
+// bf16 pairs go through the packed bf16x2 max of magnitudes.
+template <int DT>
+__device__ __forceinline__ float raw_absmax(const Raw16<DT>& r, float a) {
+  if constexpr (DT == BL_DTYPE_F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      a = fmaxf(a, fabsf(__uint_as_float(r.u[i].x)));
+      a = fmaxf(a, fabsf(__uint_as_float(r.u[i].y)));
+      a = fmaxf(a, fabsf(__uint_as_float(r.u[i].z)));
+      a = fmaxf(a, fabsf(__uint_as_float(r.u[i].w)));
+    }
+    return a;
+  } else {
+    __nv_bfloat162 m2 = __floats2bfloat162_rn(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t w[4] = {r.u[i].x, r.u[i].y, r.u[i].z, r.u[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[j])));
+    }
+    return fmaxf(a, fmaxf(__low2float(m2), __high2float(m2)));
+  }
+}
+
+__device__ __forceinline__ void team_sync(int team, int TW) {
+  if (TW == 1) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync %0, %1;" ::"r"(team + 1), "r"(TW * 32) : "memory");
+  }
+}
+
+template <int DT, int LAYOUT, bool NORM, int TW>
+__global__ void __launch_bounds__(kThreads) quant_team_kernel(const void* __restrict__ X, int M, int K, float eps,
+                                                              const float* __restrict__ gain, float eps_norm,
+                                                              double inv_k, void* __restrict__ qout,
+                                                              float* __restrict__ m_out) {
+  constexpr int kTeams = kThreads / 32 / TW;
+  constexpr int GMAX = kTeamGroups<DT>;
+  constexpr size_t kEs = DT == BL_DTYPE_F32 ? 4 : 2;
+  constexpr size_t kQs = LAYOUT == static_cast<int>(QLayout::kRowMajorI8) ? 1 : 2;
+  __shared__ float s_red[kTeams][TW];
+  __shared__ F2 s_ss[kTeams][TW];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TW, wt = warp - team * TW, tt = threadIdx.x - team * TW * 32;
+  const int row = blockIdx.x * kTeams + team;
+  pdl_wait();
+  pdl_trigger();
+  if (row >= M) return;                            // whole teams leave together
+  const int G = K >> 4;
+  const void* xr = static_cast<const char*>(X) + static_cast<size_t>(row) * K * kEs;
+  Raw16<DT> raw[GMAX];
+#pragma unroll
+  for (int i = 0; i < GMAX; ++i)
+    if (tt + i * TW * 32 < G) load_raw<DT>(xr, tt + i * TW * 32, raw[i]);
+  float a = 0.0f;
+  SumSq<DT == BL_DTYPE_BF16> ss0, ss1;
+#pragma unroll
+  for (int i = 0; i < GMAX; ++i) {
+    const int g = tt + i * TW * 32;
+    if (g < G) {
+      if constexpr (NORM) {
+        float v[16];
+        widen_raw<DT>(raw[i], v);
+        stat_group<DT, NORM>(v, g, gain, ss0, ss1, a);
+      } else {
+        a = raw_absmax<DT>(raw[i], a);
+      }
+    }
+  }
+  a = warp_max(a);
+  F2 d = {0.0f, 0.0f};
+  if constexpr (NORM) d = warp_sum_f2(f2_add({ss0.p, ss0.s}, {ss1.p, ss1.s}));
+  if (TW > 1) {
+    if (lane == 0) {
+      s_red[team][wt] = a;
+      if constexpr (NORM) s_ss[team][wt] = d;
+    }
+    team_sync(team, TW);
+#pragma unroll
+    for (int w = 0; w < TW; ++w) a = fmaxf(a, s_red[team][w]);
+  }
+  const float m = fmaxf(a, eps);
+  const float s127 = __fmul_rn(127.0f, __frcp_rn(m));
+  void* qrow = static_cast<char*>(qout) + static_cast<size_t>(row) * K * kQs;
+#pragma unroll
+  for (int i = 0; i < GMAX; ++i) {
+    const int g = tt + i * TW * 32;
+    if (g < G) {
+      float v[16];
+      widen_raw<DT>(raw[i], v);
+      if constexpr (NORM) apply_gain(gain, g, v);
+      store_group<LAYOUT>(v, g, m, s127, qrow);
+    }
+  }
+  if (tt == 0) {
+    if constexpr (NORM) {
+      F2 S = TW > 1 ? s_ss[team][0] : d;
+#pragma unroll
+      for (int w = 1; w < TW; ++w) S = f2_add(S, s_ss[team][w]);
+      m_out[row] = __double2float_rn(__dmul_rn(static_cast<double>(m), rms_factor(S, inv_k, eps_norm)));
+    } else {
+      m_out[row] = m;
+    }
+  }
+}
+
+// Warps per team for rows of K columns (0: the row is too long for a team).
+template <int DT>
+int team_warps(int K) {
+  const int G = K >> 4;
+  for (int tw = 1; tw <= 8; tw *= 2)
+    if (G <= tw * 32 * kTeamGroups<DT>) return tw;
+  return 0;
 }
 
 // Row-major int8 quantization of the token rows of several problems in one
@@ -281,9 +458,36 @@ cudaError_t launch_t(const void* X, int M, int K, float eps, const RmsNorm* norm
                             NORM ? norm->eps_norm : 0.0f, 1.0 / static_cast<double>(K), q, m_out);
 }
 
+template <int DT, int LAYOUT, bool NORM, int TW>
+cudaError_t launch_team(const void* X, int M, int K, float eps, const RmsNorm* norm, void* q, float* m_out, bool pdl,
+                        cudaStream_t st) {
+  constexpr int kTeams = kThreads / 32 / TW;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((M + kTeams - 1) / kTeams));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, quant_team_kernel<DT, LAYOUT, NORM, TW>, X, M, K, eps, NORM ? norm->g : nullptr,
+                            NORM ? norm->eps_norm : 0.0f, 1.0 / static_cast<double>(K), q, m_out);
+}
+
 template <int DT, int LAYOUT, bool NORM>
 cudaError_t launch_r(const void* X, int M, int K, float eps, const RmsNorm* norm, void* q, float* m_out, bool pdl,
                      cudaStream_t st) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // fewer rows than SMs: one CTA per row puts more threads on each row
+  switch (M >= sms ? team_warps<DT>(K) : 0) {
+    case 1: return launch_team<DT, LAYOUT, NORM, 1>(X, M, K, eps, norm, q, m_out, pdl, st);
+    case 2: return launch_team<DT, LAYOUT, NORM, 2>(X, M, K, eps, norm, q, m_out, pdl, st);
+    case 4: return launch_team<DT, LAYOUT, NORM, 4>(X, M, K, eps, norm, q, m_out, pdl, st);
+    case 8: return launch_team<DT, LAYOUT, NORM, 8>(X, M, K, eps, norm, q, m_out, pdl, st);
+    default: break;
+  }
   switch (resident_groups(K)) {
     case 1: return launch_t<DT, LAYOUT, NORM, 1>(X, M, K, eps, norm, q, m_out, pdl, st);
     case 2: return launch_t<DT, LAYOUT, NORM, 2>(X, M, K, eps, norm, q, m_out, pdl, st);

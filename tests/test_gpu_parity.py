@@ -100,20 +100,37 @@ def test_quant_act_f32_and_bf16():
     np.testing.assert_array_equal(host(m), m_ref)
 
 
-def test_quant_act_many_rows_one_warp_per_row():
-    # 300 rows take the one-warp-per-row kernel; bf16 and fp32, both layouts
-    xb = WL.batched_activations_bf16(300, 2560, seed=33)
-    Xb = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
-    q_ref, m_ref = O.quant_act(O.bf16_bits_to_f32(xb))
-    q, m = BL.quant_act(Xb)
+def _tc_to_row_major(act, M, K):
+    # fp16 slot s of a 16-column group holds column (s >> 1) + 8 * (s & 1)
+    return act.astype(np.int32).reshape(M, K // 16, 8, 2).transpose(0, 1, 3, 2).reshape(M, K)
+
+
+@pytest.mark.parametrize("M,K,dtype", [(296, 2560, "bf16"), (1000, 6912, "f32"), (3001, 2560, "f32"),
+                                       (300, 16384, "f32"), (300, 65536, "bf16")])
+def test_quant_act_many_rows(M, K, dtype):
+    # From 2 rows per SM the rows stream through a shared-memory ring (4 slots
+    # for rows up to 8 KB, 3 up to 16 KB, 2 up to 64 KB); longer rows keep one
+    # CTA per row. Both layouts; the SubLN variant with a gain as well.
+    if dtype == "bf16":
+        xb = WL.batched_activations_bf16(M, K, seed=33 + M)
+        Xd = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        X = O.bf16_bits_to_f32(xb)
+    else:
+        X = WL.prefill_activations(M, K, seed=34 + M)
+        X[5] = 0.0
+        Xd = dev(X)
+    q_ref, m_ref = O.quant_act(X)
+    q, m = BL.quant_act(Xd)
     np.testing.assert_array_equal(host(q), q_ref)
     np.testing.assert_array_equal(host(m).view(np.uint32), m_ref.view(np.uint32))
-    X = WL.prefill_activations(300, 6912, seed=34)
-    q_ref, m_ref = O.quant_act(X)
-    act, m = BL.quant_act_tc(dev(X))
-    np.testing.assert_array_equal(host(act).astype(np.int32).reshape(300, 6912 // 16, 8, 2).transpose(0, 1, 3, 2)
-                                  .reshape(300, 6912), q_ref)
+    act, m = BL.quant_act_tc(Xd)
+    np.testing.assert_array_equal(_tc_to_row_major(host(act), M, K), q_ref)
     np.testing.assert_array_equal(host(m).view(np.uint32), m_ref.view(np.uint32))
+    g = WL.norm_gain(K, seed=35 + M)
+    q, m = BL.rmsnorm_quant(Xd, dev(g))
+    q_ref, m_ref = O.rmsnorm_quant(X, g)
+    np.testing.assert_array_equal(host(q), q_ref)
+    assert_m_close(host(m), m_ref)
 
 
 # ----------------------------------------------------------------- forward
