@@ -390,7 +390,7 @@ def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096
     quantization + tensor-core GEMM; and the GEMM alone on a pre-quantized
     input) and through the fused FFN block 2560 -> 6912 -> ReLU^2 -> 2560."""
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
-    out = {"M": M, "unit": "TOPS", "forward": {}, "gemm_only": {}, "ms": {}}
+    out = {"M": M, "unit": "TOPS", "forward": {}, "forward_rmsnorm": {}, "gemm_only": {}, "ms": {}}
     ws = BL.Workspace(0, device)
     best, best_shape = None, None
     with torch.cuda.stream(stream):
@@ -409,9 +409,14 @@ def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096
             t_fwd = time_each(torch, lambda: BL.forward(X, packed, s_w, out=Y, workspace=ws), iters, stream, flush)
             t_mm = time_each(torch, lambda: BL.forward_tc(act, m, packed, s_w, out=Y, workspace=ws), iters, stream,
                              flush)
+            g = torch.from_numpy(WL.norm_gain(K, seed=9200 + K, edge=False)).to(device)
+            t_norm = time_each(torch, lambda: BL.forward_rmsnorm(X, packed, s_w, g, out=Y, workspace=ws), iters,
+                               stream, flush)
             out["forward"][shape] = round(ops / t_fwd / 1e12, 1)
+            out["forward_rmsnorm"][shape] = round(ops / t_norm / 1e12, 1)
             out["gemm_only"][shape] = round(ops / t_mm / 1e12, 1)
-            out["ms"][shape] = {"forward": round(t_fwd * 1e3, 4), "gemm": round(t_mm * 1e3, 4)}
+            out["ms"][shape] = {"forward": round(t_fwd * 1e3, 4), "forward_rmsnorm": round(t_norm * 1e3, 4),
+                                "gemm": round(t_mm * 1e3, 4)}
             if shape == "up" or best is None:
                 best, best_shape = (ops, t_mm), shape
             del X, Y, act, m, packed
@@ -426,8 +431,20 @@ def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096
             torch.cuda.synchronize()
             t_ffn = time_each(torch, lambda: BL.ffn(X, up, s_up, down, s_down, out=Yf, workspace=ws), iters,
                               stream, flush)
+            gate, s_gate = BL.pack(torch.from_numpy(WL.decode_weights("up", 2)).to(device))
+            g_in = torch.from_numpy(WL.norm_gain(D, seed=9300, edge=False)).to(device)
+            g_sub = torch.from_numpy(WL.norm_gain(F, seed=9301, edge=False)).to(device)
+            t_gated = time_each(torch, lambda: BL.ffn_gated(X, up, s_up, gate, s_gate, down, s_down, out=Yf,
+                                                            workspace=ws), iters, stream, flush)
+            t_subln = time_each(torch, lambda: BL.ffn_subln(X, up, s_up, down, s_down, g_in=g_in, g_sub=g_sub,
+                                                            gate=gate, s_gate=s_gate, out=Yf, workspace=ws),
+                                iters, stream, flush)
         out["ffn"] = round(4.0 * M * D * F / t_ffn / 1e12, 1)
+        out["ffn_gated"] = round(6.0 * M * D * F / t_gated / 1e12, 1)
+        out["ffn_subln_gated"] = round(6.0 * M * D * F / t_subln / 1e12, 1)
         out["ms"]["ffn"] = round(t_ffn * 1e3, 4)
+        out["ms"]["ffn_gated"] = round(t_gated * 1e3, 4)
+        out["ms"]["ffn_subln_gated"] = round(t_subln * 1e3, 4)
     ops, t_mm = best
     achieved = ops / t_mm / 1e12
     up_name = "FFN up 2560->6912" if best_shape == "up" else best_shape
@@ -440,7 +457,8 @@ def prefill_leg(torch, BL, WL, device, peaks, peak_src, stream, iters=20, M=4096
                        "how": "one bitlinear_forward_tc launch per timed call (CUDA events on the launching "
                               "stream), L2 flushed between calls"}
     out["how"] = ("integer-valued fp16 operands on tcgen05 kind::f16 (sm_103a has no int8 tcgen05 MMA); "
-                  "ops = 2*M*N*K per projection, 4*M*D*F for the FFN")
+                  "ops = 2*M*N*K per projection, 4*M*D*F for the FFN, 6*M*D*F gated; forward_rmsnorm and "
+                  "ffn_subln_gated include the fused RMSNorm (unit-scale gains)")
     return out
 
 

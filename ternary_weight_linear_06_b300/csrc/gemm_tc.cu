@@ -455,18 +455,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* yp = p.Y + static_cast<size_t>(tok0) * p.N + n;
         int32_t* ap = ACC ? p.acc + static_cast<size_t>(tok0) * p.N + n : nullptr;
-        const float* mp = MUL ? p.mul + static_cast<size_t>(tok0) * p.N + n : nullptr;
         const int jmax = min(32, p.M - tok0);
+        // the factors of the product, all loaded before the first store (the
+        // stores to Y could otherwise alias them and serialize the loads)
+        float mv[MUL ? 32 : 1];
+        if constexpr (MUL) {
+          const float* mp = p.mul + static_cast<size_t>(tok0) * p.N + n;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mv[j] = (j < jmax && n_ok) ? __ldg(mp + static_cast<size_t>(j) * p.N) : 0.0f;
+        }
         if (jmax == 32 && n_ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float accf = __uint_as_float(v[j]);
             float y = __fmul_rn(accf, __shfl_sync(0xffffffffu, my_c, j));
             if constexpr (RELU2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
-            if constexpr (MUL) {
-              y = __fmul_rn(y, *mp);
-              mp += p.N;
-            }
+            if constexpr (MUL) y = __fmul_rn(y, mv[j]);
             *yp = y;
             yp += p.N;
             if constexpr (ACC) {
@@ -481,13 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             float y = __fmul_rn(accf, __shfl_sync(0xffffffffu, my_c, j));
             if constexpr (RELU2) y = y > 0.0f ? __fmul_rn(y, y) : 0.0f;
             if (j < jmax && n_ok) {
-              if constexpr (MUL) y = __fmul_rn(y, *mp);
+              if constexpr (MUL) y = __fmul_rn(y, mv[j]);
               *yp = y;
               if constexpr (ACC) *ap = __float2int_rn(accf);
             }
             yp += p.N;
             if constexpr (ACC) ap += p.N;
-            if constexpr (MUL) mp += p.N;
           }
         }
       }
