@@ -17,7 +17,7 @@ Multi-GPU (torchrun): each rank runs an independent replica (weak scaling);
 value = all ranks' bytes / the slowest rank's time.
 
 --impl reference times the CPU oracle on a bounded sample of the same
-workload (the oracle is the reference for this build; it is not tuned).
+workload (the oracle is the reference arm; it is not tuned).
 """
 from __future__ import annotations
 

@@ -48,38 +48,34 @@ bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CU
 // bitlinear_forward_tc for any count).
 bool uses_split(int M, int N, int K) { return gemm_splits(M, N, K) > 1; }
 
-// Forward workspace: header | q (M*K fp16 or int8) | m [M] | qsum [M] | split-K sums [M*N] int32
+// Forward workspace: header | q (M*K fp16 or int8) | m [M] | split-K sums [M*N] int32
 // Batch workspace: header | q of every problem (M_p * K_p int8 each) | m of every problem
 struct FwdLayout {
-  size_t q, m, qsum, accw, total;
+  size_t q, m, accw, total;
 };
 FwdLayout fwd_layout(int M, int N, int K) {
   FwdLayout L;
   L.q = sizeof(WsHeader);
   L.m = align_up(L.q + static_cast<size_t>(M) * K * 2, 256);
-  L.qsum = align_up(L.m + 4 * static_cast<size_t>(M), 256);
-  L.accw = align_up(L.qsum + 4 * static_cast<size_t>(M), 256);
+  L.accw = align_up(L.m + 4 * static_cast<size_t>(M), 256);
   L.total = uses_split(M, N, K) ? align_up(L.accw + 4 * static_cast<size_t>(M) * N, 256) : L.accw;
   return L;
 }
 
-// FFN workspace: header | qx | mx | qsx | h [M*F] | hmax [M] | qh | mh | qsh | split-K sums
+// FFN workspace: header | qx | mx | h [M*F] fp32 | qh | mh | split-K sums
 // (gated: then ReLU^2(gate) [M*F] after the split-K sums)
 struct FfnLayout {
-  size_t qx, mx, qsx, h, hmax, qh, mh, qsh, accw, g, total;
+  size_t qx, mx, h, qh, mh, accw, g, total;
 };
 FfnLayout ffn_layout(int M, int D, int F, bool gated = false) {
   FfnLayout L;
   const size_t m4 = 4 * static_cast<size_t>(M);
   L.qx = sizeof(WsHeader);
   L.mx = align_up(L.qx + static_cast<size_t>(M) * D * 2, 256);
-  L.qsx = align_up(L.mx + m4, 256);
-  L.h = align_up(L.qsx + m4, 256);
-  L.hmax = align_up(L.h + static_cast<size_t>(M) * F * 4, 256);
-  L.qh = align_up(L.hmax + m4, 256);
+  L.h = align_up(L.mx + m4, 256);
+  L.qh = align_up(L.h + static_cast<size_t>(M) * F * 4, 256);
   L.mh = align_up(L.qh + static_cast<size_t>(M) * F * 2, 256);
-  L.qsh = align_up(L.mh + m4, 256);
-  L.accw = align_up(L.qsh + m4, 256);
+  L.accw = align_up(L.mh + m4, 256);
   const bool split = uses_split(M, F, D) || uses_split(M, D, F);
   L.g = split ? align_up(L.accw + 4 * static_cast<size_t>(M) * std::max(D, F), 256) : L.accw;
   L.total = gated ? align_up(L.g + 4 * static_cast<size_t>(M) * F, 256) : L.g;

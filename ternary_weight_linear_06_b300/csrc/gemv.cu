@@ -26,9 +26,9 @@
 //      same activation chunk at the same time (a shared-memory broadcast);
 //   3. the LPR partial sums of a row meet by warp shuffles and one lane per
 //      token writes y.
-// LPR is picked per problem so that the K/64 chunks of a row split evenly
-// over the group's lanes (K = 2560: 40 chunks, 8 lanes; K = 6912: 108
-// chunks, 4 lanes).
+// LPR is picked per problem by a cost model (a warp's item costs about its
+// chunks per lane plus one): 4 lanes for every 2B- and 70B-class row; a
+// launch with too few rows to give every warp two items widens the groups.
 //
 // Packed rows are K/4 bytes (code t+1 of column 4b+j in bits [2j,2j+1] of byte
 // b): in a 32-bit word the code of column 16w+4j+i sits at bit 8j+2i. The

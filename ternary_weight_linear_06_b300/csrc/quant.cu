@@ -5,12 +5,13 @@
 // the 2B4T report (section 2) applies absmax per token. With Qb = 127:
 //   m = max(max_k |x_k|, eps);  q_k = clamp(rint(fp32(fp32(x_k * 127) / m)), -128, 127).
 //
-// One CTA per token row: pass 1 reduces |x| to the row absmax, pass 2
-// quantizes 16 columns per thread step and writes them in the layout the
-// consumer wants (row-major int8, or fp16 in the tensor-core operand order).
-// Rows up to 16384 columns stay in registers between the passes.
-// A batched variant quantizes the token rows of up to kQuantMaxBatch
-// problems in one launch.
+// Pass 1 reduces |x| to the row absmax, pass 2 quantizes 16 columns per
+// thread step and writes them in the layout the consumer wants (row-major
+// int8, or fp16 in the tensor-core operand order). From one row per SM up, a
+// team of 1-8 warps takes a row (several teams per CTA); fewer rows get one
+// CTA each. Rows up to 16384 columns stay in registers between the passes. A
+// batched variant quantizes the token rows of up to kQuantMaxBatch problems
+// in one launch.
 //
 // SubLN ("BitNet b1.58 2B4T Technical Report", section 2: a sub-layer norm,
 // bias-free norm layers; RMSNorm as the LLaMA-style norm in "BitNet解读",
@@ -34,7 +35,7 @@ constexpr int kThreads = 256;
 // Dot Product", SIAM J. Sci. Comput. 26(6), 2005): each square is split
 // exactly into its rounded value and the FMA remainder, each addition into its
 // rounded sum and the TwoSum error. The pair holds the sum to about twice
-// fp32's precision without the fp64 pipe, which is slow on this GPU. With
+// fp32's precision without the fp64 pipe, which is slow on B300. With
 // EXACT_SQ (bf16 inputs: an 8-bit significand squares exactly in fp32) the
 // FMA remainder is known to be zero and skipped.
 struct F2 {
