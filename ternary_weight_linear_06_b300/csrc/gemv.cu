@@ -141,6 +141,47 @@ __device__ void stage_all(const BatchArgs<CAP>& a, Span<MT>* spans, int nspan, u
   __syncthreads();
 }
 
+// One batch of up to U chunks of a lane's row: loads issued together, then
+// consumed. FULL: all U chunks exist (no per-chunk checks).
+template <int MT, int LPR, int U, bool FULL>
+__device__ __forceinline__ void gemv_batch(const uint4* wrow, int c0, int lim, bool valid, const uint4* a0, int C,
+                                           int (&acc)[MT][MT == 1 ? 4 : 1]) {
+  uint4 w[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if constexpr (FULL) w[u] = __ldg(wrow + c0 + u * LPR);
+    else w[u] = (valid && u * LPR < lim) ? __ldg(wrow + c0 + u * LPR) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (!FULL && u * LPR >= lim) break;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t wv = j == 0 ? w[u].x : j == 1 ? w[u].y : j == 2 ? w[u].z : w[u].w;
+      if constexpr (MT == 1) {
+        const uint4 av = a0[j * C + u * LPR];
+        acc[0][0] = dp4a_su(static_cast<int>(av.x), wv & 0x03030303u, acc[0][0]);
+        acc[0][1] = dp4a_su(static_cast<int>(av.y), wv & 0x0C0C0C0Cu, acc[0][1]);
+        acc[0][2] = dp4a_su(static_cast<int>(av.z), wv & 0x30303030u, acc[0][2]);
+        acc[0][3] = dp4a_su(static_cast<int>(av.w), wv & 0xC0C0C0C0u, acc[0][3]);
+      } else {
+        const uint32_t x0 = wv & 0x03030303u, x1 = (wv >> 2) & 0x03030303u;
+        const uint32_t x2 = (wv >> 4) & 0x03030303u, x3 = (wv >> 6) & 0x03030303u;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const uint4 av = a0[(t * 4 + j) * C + u * LPR];
+          int s = acc[t][0];
+          s = dp4a_su(static_cast<int>(av.x), x0, s);
+          s = dp4a_su(static_cast<int>(av.y), x1, s);
+          s = dp4a_su(static_cast<int>(av.z), x2, s);
+          s = dp4a_su(static_cast<int>(av.w), x3, s);
+          acc[t][0] = s;
+        }
+      }
+    }
+  }
+}
+
 // One warp's share of a span: items (32/LPR rows each, one row per lane
 // group) it = it0, it0 + kWarps, ... A row's C chunks are read in batches of
 // up to U chunks per lane; the U loads of a batch are issued together, then
@@ -154,8 +195,8 @@ __device__ __forceinline__ void run_span(const DevProb& P, const Span<MT>& S, co
   const int C = P.K >> 6;
   const int n_per = (C + LPR - 1) / LPR;               // chunks per lane per row
   const int nb = (n_per + U - 1) / U;                  // batches per row
-  // full batches first (measured: more loads in flight beats an even split)
-  const int Ue = U;
+  // full batches first (measured: more loads in flight beats an even split);
+  // a lane whose batch is complete skips the per-chunk checks
   const int r0 = S.r0, r1 = S.r1;
   const int n_items = (r1 - r0 + G - 1) / G;
   const size_t rb = static_cast<size_t>(P.K) >> 2;
@@ -169,41 +210,10 @@ __device__ __forceinline__ void run_span(const DevProb& P, const Span<MT>& S, co
 #pragma unroll
       for (int i = 0; i < NA; ++i) acc[t][i] = 0;
     for (int b = 0; b < nb; ++b) {
-      const int c0 = b * (LPR * Ue) + sub;
-      const int lim = C - c0;                 // chunk u exists when u < Ue and u * LPR < lim
-      uint4 w[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        w[u] = (valid && u < Ue && u * LPR < lim) ? __ldg(wrow + c0 + u * LPR) : make_uint4(0u, 0u, 0u, 0u);
-      const uint4* a0 = act + c0;
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (u >= Ue || u * LPR >= lim) break;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t wv = j == 0 ? w[u].x : j == 1 ? w[u].y : j == 2 ? w[u].z : w[u].w;
-          if constexpr (MT == 1) {
-            const uint4 av = a0[j * C + u * LPR];
-            acc[0][0] = dp4a_su(static_cast<int>(av.x), wv & 0x03030303u, acc[0][0]);
-            acc[0][1] = dp4a_su(static_cast<int>(av.y), wv & 0x0C0C0C0Cu, acc[0][1]);
-            acc[0][2] = dp4a_su(static_cast<int>(av.z), wv & 0x30303030u, acc[0][2]);
-            acc[0][3] = dp4a_su(static_cast<int>(av.w), wv & 0xC0C0C0C0u, acc[0][3]);
-          } else {
-            const uint32_t x0 = wv & 0x03030303u, x1 = (wv >> 2) & 0x03030303u;
-            const uint32_t x2 = (wv >> 4) & 0x03030303u, x3 = (wv >> 6) & 0x03030303u;
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-              const uint4 av = a0[(t * 4 + j) * C + u * LPR];
-              int s = acc[t][0];
-              s = dp4a_su(static_cast<int>(av.x), x0, s);
-              s = dp4a_su(static_cast<int>(av.y), x1, s);
-              s = dp4a_su(static_cast<int>(av.z), x2, s);
-              s = dp4a_su(static_cast<int>(av.w), x3, s);
-              acc[t][0] = s;
-            }
-          }
-        }
-      }
+      const int c0 = b * (LPR * U) + sub;
+      const int lim = C - c0;                 // chunk u exists when u * LPR < lim
+      if (valid && lim > (U - 1) * LPR) gemv_batch<MT, LPR, U, true>(wrow, c0, lim, valid, act + c0, C, acc);
+      else gemv_batch<MT, LPR, U, false>(wrow, c0, lim, valid, act + c0, C, acc);
     }
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
