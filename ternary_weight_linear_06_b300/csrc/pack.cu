@@ -11,9 +11,10 @@
 //      mant << (e - 86) to a 128-bit fixed-point accumulator (unit 2^-64);
 //      the bound N*K < 2^31 keeps the grand total below 2^127. The rare
 //      values outside that window go to 64-bit per-exponent buckets.
-//   2. finalize_kernel: one thread adds the block partials and the buckets
-//      into a 352-bit integer (unit 2^-149), divides by N*K with long
-//      division and rounds to nearest-even fp32, then s_w = fp32(gamma + eps).
+//   2. finalize_kernel: the CTA adds the block partials in 128 bits, then
+//      one thread adds that sum and the buckets into a 352-bit integer (unit
+//      2^-149), divides by N*K with long division and rounds to nearest-even
+//      fp32, then s_w = fp32(gamma + eps).
 //   3. codes_kernel: one float4 -> one byte. rint(fp32(w / s)) clipped to
 //      [-1, 1] is 0 exactly when 2|w| <= s (for finite w and s > 0: the
 //      quotient rounds to at most 0.5 iff |w|/s <= 0.5 + 2^-25, and no fp32
@@ -102,19 +103,33 @@ __device__ bool any_below(const uint32_t* Q, int pos) {
   return false;
 }
 
-__global__ void finalize_kernel(PackScratch* __restrict__ sc, uint32_t nblocks, uint32_t n, float eps,
-                                float* __restrict__ s_w) {
-  if (threadIdx.x != 0) return;
+__global__ void __launch_bounds__(kSumThreads) finalize_kernel(PackScratch* __restrict__ sc, uint32_t nblocks,
+                                                                uint32_t n, float eps, float* __restrict__ s_w) {
+  // The window partials add up to less than 2^127 (N*K < 2^31), so any subset
+  // of them sums exactly in 128 bits: the CTA adds them in parallel, and the
+  // buckets are read into shared memory at the same time.
+  __shared__ unsigned __int128 red[kSumThreads];
+  __shared__ unsigned long long s_bucket[256];
+  const int tid = threadIdx.x;
+  unsigned __int128 part = 0;
+  for (uint32_t b = tid; b < nblocks; b += kSumThreads)
+    part += (static_cast<unsigned __int128>(sc->partial[b][1]) << 64) | sc->partial[b][0];
+  red[tid] = part;
+  for (int e = tid; e < 256; e += kSumThreads) s_bucket[e] = sc->bucket[e];
+  __syncthreads();
+  for (int st = kSumThreads / 2; st > 0; st >>= 1) {
+    if (tid < st) red[tid] += red[tid + st];
+    __syncthreads();
+  }
+  if (tid != 0) return;
   unsigned long long limb[kLimbs + 2];
   for (int i = 0; i < kLimbs + 2; ++i) limb[i] = 0;
-  // window partials: value = P * 2^-64 = P * 2^85 in units of 2^-149
-  for (uint32_t b = 0; b < nblocks; ++b) {
-    big_add(limb, sc->partial[b][0], 85);
-    big_add(limb, sc->partial[b][1], 85 + 64);
-  }
+  // window sum: value = P * 2^-64 = P * 2^85 in units of 2^-149
+  big_add(limb, static_cast<unsigned long long>(red[0]), 85);
+  big_add(limb, static_cast<unsigned long long>(red[0] >> 64), 85 + 64);
   // buckets: value = S * 2^(e-150) = S * 2^(e-1) in units of 2^-149
   for (int e = 1; e < 255; ++e)
-    if (sc->bucket[e]) big_add(limb, sc->bucket[e], e - 1);
+    if (s_bucket[e]) big_add(limb, s_bucket[e], e - 1);
   uint32_t S[kLimbs];
   unsigned long long carry = 0;
   for (int i = 0; i < kLimbs; ++i) {
@@ -212,7 +227,8 @@ cudaError_t launch_pack(const float* W, int N, int K, float eps, uint8_t* packed
   cudaError_t err = cudaMemsetAsync(sc, 0, sizeof(PackScratch), st);
   if (err != cudaSuccess) return err;
   abs_sum_kernel<<<blocks, kSumThreads, 0, st>>>(reinterpret_cast<const uint4*>(W), n4, sc);
-  finalize_kernel<<<1, 32, 0, st>>>(sc, static_cast<uint32_t>(blocks), static_cast<uint32_t>(static_cast<size_t>(N) * K), eps, s_w);
+  finalize_kernel<<<1, kSumThreads, 0, st>>>(sc, static_cast<uint32_t>(blocks),
+                                             static_cast<uint32_t>(static_cast<size_t>(N) * K), eps, s_w);
   const int cblocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, static_cast<size_t>(16 * nsm)));
   codes_kernel<<<cblocks, 256, 0, st>>>(reinterpret_cast<const float4*>(W), n4, s_w, packed);
   return cudaGetLastError();
