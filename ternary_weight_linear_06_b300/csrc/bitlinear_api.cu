@@ -152,10 +152,18 @@ bl_status run_forward(const void* X, int x_dtype, int M, int K, const RmsNorm* n
     return from_cuda(launch_gemm(make_gemm(M, K, packed, s_w, N, act, m, Y, acc, false, at<int32_t>(workspace, L.accw)),
                                  static_cast<WsHeader*>(workspace), true, st));
   }
+  GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
+  if (norm == nullptr) {
+    // decode without a norm: the GEMV quantizes its few token rows while
+    // staging them (one launch instead of two in a chain of dependent calls)
+    p.x = X;
+    p.x_dtype = x_dtype;
+    p.eps = eps;
+    return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));
+  }
   int8_t* q = at<int8_t>(workspace, L.q);
   if (launch_quant(X, x_dtype, M, K, eps, QLayout::kRowMajorI8, q, m, norm, true, st) != cudaSuccess)
     return BL_ERR_CUDA;
-  GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
   p.q = q;
   p.m = m;
   return from_cuda(launch_gemv(p, static_cast<WsHeader*>(workspace), true, st));

@@ -68,6 +68,9 @@ struct DevProb {
   float* Y;
   int32_t* acc;
   const float* mul;       // [M][N] or null: y = fp32(y * mul)
+  const void* x;          // raw activations [M][K] when the launch quantizes them itself
+  int x_dtype;
+  float eps;
   int N, K, M;
   int epi;
   int lpr;                // lanes per row
@@ -81,6 +84,7 @@ struct BatchArgs {
   unsigned char cta_p0[kMaxCtas];   // the problem holding row cta_row[c]
   int count;
   int t0;                           // tokens t0 .. t0+MT-1 of every problem
+  int from_x;                       // quantize the token rows from DevProb::x while staging
 };
 
 // What one CTA knows about a problem its run touches.
@@ -109,9 +113,33 @@ __device__ __forceinline__ uint4 to_quad(uint4 v) {
 // into the order above. The sums of codes meet in shared memory by atomics;
 // then each token's dequant factor is computed once.
 template <int MT, int CAP>
-__device__ void stage_all(const BatchArgs<CAP>& a, Span<MT>* spans, int nspan, uint4* s_act, int* s_qs) {
+__device__ void stage_all(const BatchArgs<CAP>& a, Span<MT>* spans, int nspan, uint4* s_act, int* s_qs,
+                          unsigned* s_amax) {
   const int tid = threadIdx.x;
   const int total = spans[nspan - 1].act + MT * (a.prob[spans[nspan - 1].p].K >> 4);
+  if (a.from_x) {
+    // per-token absmax of the raw rows first (non-negative floats order like
+    // their bit patterns, so an integer max reduces them exactly)
+    int j = 0;
+    for (int g = tid; g < total; g += kThreads) {
+      while (j + 1 < nspan && spans[j + 1].act <= g) ++j;
+      const DevProb& P = a.prob[spans[j].p];
+      const int K16 = P.K >> 4;
+      const int local = g - spans[j].act;
+      const int t = local / K16, gg = local - t * K16;
+      if (a.t0 + t < P.M) {
+        float v[16];
+        const size_t off = static_cast<size_t>(a.t0 + t) * P.K;
+        if (P.x_dtype == BL_DTYPE_F32) load16<BL_DTYPE_F32>(static_cast<const float*>(P.x) + off, gg, v);
+        else load16<BL_DTYPE_BF16>(static_cast<const uint16_t*>(P.x) + off, gg, v);
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, fabsf(v[i]));
+        atomicMax(&s_amax[j * MT + t], __float_as_uint(mx));
+      }
+    }
+    __syncthreads();
+  }
   int j = 0;
   for (int g = tid; g < total; g += kThreads) {
     while (j + 1 < nspan && spans[j + 1].act <= g) ++j;
@@ -121,7 +149,23 @@ __device__ void stage_all(const BatchArgs<CAP>& a, Span<MT>* spans, int nspan, u
     const int t = local / K16, gg = local - t * K16;
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
     if (a.t0 + t < P.M) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(P.q + static_cast<size_t>(a.t0 + t) * P.K) + gg);
+      uint4 v;
+      if (a.from_x) {
+        // the same codes as the quantization kernel: m = max(absmax, eps)
+        const float m = fmaxf(__uint_as_float(s_amax[j * MT + t]), P.eps);
+        const float s127 = __fmul_rn(127.0f, __frcp_rn(m));
+        float f[16];
+        const size_t off = static_cast<size_t>(a.t0 + t) * P.K;
+        if (P.x_dtype == BL_DTYPE_F32) load16<BL_DTYPE_F32>(static_cast<const float*>(P.x) + off, gg, f);
+        else load16<BL_DTYPE_BF16>(static_cast<const uint16_t*>(P.x) + off, gg, f);
+        int c[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c[i] = static_cast<int>(quant_round(f[i], m, s127));
+        v = make_uint4(pack4(c[0], c[1], c[2], c[3]), pack4(c[4], c[5], c[6], c[7]), pack4(c[8], c[9], c[10], c[11]),
+                       pack4(c[12], c[13], c[14], c[15]));
+      } else {
+        v = __ldg(reinterpret_cast<const uint4*>(P.q + static_cast<size_t>(a.t0 + t) * P.K) + gg);
+      }
       o = to_quad(v);
       int qpart = dp4a_su(static_cast<int>(v.x), 0x01010101u, 0);
       qpart = dp4a_su(static_cast<int>(v.y), 0x01010101u, qpart);
@@ -136,7 +180,9 @@ __device__ void stage_all(const BatchArgs<CAP>& a, Span<MT>* spans, int nspan, u
     const int jj = tid / MT, t = tid - jj * MT;
     const DevProb& P = a.prob[spans[jj].p];
     spans[jj].qs[t] = s_qs[tid];
-    spans[jj].c[t] = a.t0 + t < P.M ? dequant_factor(P.s_w[0], P.m_in[a.t0 + t]) : 0.0f;
+    float m = 0.0f;
+    if (a.t0 + t < P.M) m = a.from_x ? fmaxf(__uint_as_float(s_amax[tid]), P.eps) : P.m_in[a.t0 + t];
+    spans[jj].c[t] = a.t0 + t < P.M ? dequant_factor(P.s_w[0], m) : 0.0f;
   }
   __syncthreads();
 }
@@ -244,9 +290,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   __shared__ Span<MT> s_span[kMaxSpan];
   __shared__ int s_nspan;
   __shared__ int s_qs[kMaxSpan * MT];
+  __shared__ unsigned s_amax[kMaxSpan * MT];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int r_begin = a.cta_row[blockIdx.x], r_end = a.cta_row[blockIdx.x + 1];
-  if (tid < kMaxSpan * MT) s_qs[tid] = 0;
+  if (tid < kMaxSpan * MT) {
+    s_qs[tid] = 0;
+    s_amax[tid] = 0u;
+  }
   if (tid == 0) {
     int nspan = 0, items = 0, act = 0;
     if (r_begin < r_end) {
@@ -275,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gemv_kernel(const __grid
   pdl_wait();
   const int nspan = s_nspan;
   if (nspan == 0) return;
-  stage_all<MT, CAP>(a, s_span, nspan, s_act, s_qs);
+  stage_all<MT, CAP>(a, s_span, nspan, s_act, s_qs, s_amax);
   // items are dealt round-robin over the warps across all spans (item i of
   // the CTA goes to warp i % kWarps); the rows of a span are contiguous in
   // HBM, so the CTA streams one region at a time
@@ -426,6 +476,9 @@ DevProb to_dev(const GemvProblem& p) {
   d.Y = p.Y;
   d.acc = p.acc;
   d.mul = p.mul;
+  d.x = p.x;
+  d.x_dtype = p.x_dtype;
+  d.eps = p.eps;
   d.N = p.N;
   d.K = p.K;
   d.M = p.M;
@@ -445,6 +498,7 @@ cudaError_t run_tokens(const GemvProblem* ps, int count, int t0, WsHeader* statu
   if (n == 0) return cudaSuccess;
   a.count = n;
   a.t0 = t0;
+  a.from_x = (n == 1 && a.prob[0].x != nullptr) ? 1 : 0;
   return launch_batch<MT, CAP>(a, pdl, st, planned);
 }
 

@@ -57,6 +57,11 @@ struct GemvProblem {
   int32_t* acc;          // [M][N] or null
   Epi epi;
   const float* mul;      // [M][N] or null: y = fp32(y * mul) (the gated FFN's up projection)
+  // single-problem launches only: when x is set, the GEMV quantizes the token
+  // rows itself (q and m are then unused)
+  const void* x;         // [M][K] fp32 or bf16, or null
+  int x_dtype;
+  float eps;
 };
 constexpr int kGemvMaxBatch = 128;
 // One problem (M <= 4 per launch; more tokens take several launches).
