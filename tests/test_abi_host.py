@@ -26,6 +26,23 @@ def test_library_exports_every_declared_symbol():
     assert set(names) <= set(_lib.SIGNATURES), "binding misses a declared entry point"
 
 
+def _prototypes():
+    """name -> parameter count, from the BL_API declarations of the header."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"BL_API\s+[\w\s\*]+?\b(bitlinear_\w+)\s*\(([^)]*)\)\s*;", src):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_lists_match_the_header():
+    protos = _prototypes()
+    assert set(protos) == set(_declared())
+    for name, n in protos.items():
+        assert len(_lib.SIGNATURES[name][1]) == n, (name, n, len(_lib.SIGNATURES[name][1]))
+
+
 def test_version_and_status_strings():
     lib = _lib.lib()
     assert lib.bitlinear_version() == 102
