@@ -546,7 +546,7 @@ def run_crossover(args):
     stream = torch.cuda.Stream(device)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     ws = BL.Workspace(0, device)
-    Ms = [1, 2, 4, 8, 12, 16, 24, 32, 48, 64, 128, 256]
+    Ms = [1, 2, 4, 5, 6, 8, 12, 16, 24, 32, 48, 64, 128, 256]
     out = {"what": "batched decode: GEMV vs tensor-core GEMM (us per call, L2 flushed)", "M": Ms, "shapes": {}}
     with torch.cuda.stream(stream):
         for shape in SHAPE_ORDER:

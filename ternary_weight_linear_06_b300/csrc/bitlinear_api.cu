@@ -48,6 +48,12 @@ bl_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BL_OK : BL_ERR_CU
 // bitlinear_forward_tc for any count).
 bool uses_split(int M, int N, int K) { return gemm_splits(M, N, K) > 1; }
 
+// A single GEMV launch (up to 4 tokens) quantizes its raw rows in-kernel when
+// they hold at most this many values; measured on B300, the staging of 4 rows
+// of 8192 fp32 values in every CTA cost more than the launch it saves.
+constexpr int kGemvInKernelQuantTokens = 4;
+constexpr int kGemvInKernelQuantElems = 16384;
+
 // Forward workspace: header | q (M*K fp16 or int8) | m [M] | split-K sums [M*N] int32
 // Batch workspace: header | q of every problem (M_p * K_p int8 each) | m of every problem
 struct FwdLayout {
@@ -153,9 +159,11 @@ bl_status run_forward(const void* X, int x_dtype, int M, int K, const RmsNorm* n
                                  static_cast<WsHeader*>(workspace), true, st));
   }
   GemvProblem p = make_problem(M, K, packed, s_w, N, Y, acc);
-  if (norm == nullptr) {
-    // decode without a norm: the GEMV quantizes its few token rows while
-    // staging them (one launch instead of two in a chain of dependent calls)
+  if (norm == nullptr && M <= kGemvInKernelQuantTokens && M * K <= kGemvInKernelQuantElems) {
+    // decode without a norm, few short rows: the GEMV quantizes them while
+    // staging (one launch instead of two in a chain of dependent calls);
+    // every CTA reads the raw rows twice, so longer or more rows go through
+    // the quantization kernel once
     p.x = X;
     p.x_dtype = x_dtype;
     p.eps = eps;

@@ -86,9 +86,10 @@ struct GemmProblem {
 // need an [M][N] int32 scratch (GemmProblem::acc_ws).
 int gemm_splits(int M, int N, int K);
 // Tokens from which the forward takes the tensor-core GEMM instead of the GEMV
-// (measured on B300: the GEMV is faster up to 8 tokens on the 2B-class shapes,
-// the GEMM from 12).
-constexpr int kGemmMinTokens = 9;
+// (measured on B300, each call alone with L2 flushed: at 4 tokens the GEMV is
+// faster on every 2B-class shape, from 5 the GEMM, whose split-K time is flat;
+// the GEMV takes at most 4 tokens per launch, so 5 tokens need two).
+constexpr int kGemmMinTokens = 5;
 cudaError_t launch_gemm(const GemmProblem& g, WsHeader* status, bool pdl, cudaStream_t st);
 
 }  // namespace bl

@@ -312,7 +312,7 @@ def test_forward_long_k_and_tiny_n():
         check_forward(W, X)
 
 
-# ------------------------------------------------- tensor-core GEMM (M >= 9)
+# ------------------------------------------------- tensor-core GEMM (M >= 5)
 @pytest.mark.parametrize("M,K,N", [(17, 64, 128), (64, 320, 203), (128, 2560, 640), (129, 576, 130),
                                    (300, 2560, 257), (1000, 128, 384)])
 def test_gemm_path_ragged_tiles(M, K, N):
