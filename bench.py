@@ -164,7 +164,7 @@ def build_decode(torch, BL, WL, layers: int, device):
 # capture summarised in profiles/gemv_batch_decode_m1_x12.md (12 layers). They
 # hold only for the kernel source they were taken on: a changed gemv.cu gives
 # traffic = null until it is profiled again.
-TRAFFIC = {"source": "ternary_weight_linear_06_b300/csrc/gemv.cu", "sha256_prefix": "d6e3fc28cdbed42e",
+TRAFFIC = {"source": "ternary_weight_linear_06_b300/csrc/gemv.cu", "sha256_prefix": "dcebfd9a1121beeb",
            "bytes": 135634432.0, "layers": 12}
 
 

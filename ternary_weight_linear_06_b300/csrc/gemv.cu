@@ -7,7 +7,9 @@
 // is additions and subtractions of activations.
 //
 // The activations arrive quantized (int8, row-major, with their per-token
-// absmax m) from the quantization kernel that precedes this one.
+// scale m) from the quantization kernel that precedes this one, or, for a
+// single problem of a few short rows, raw (fp32/bf16): the CTAs then quantize
+// them while staging, with the quantization kernel's code rule.
 //
 // Work split. The rows of all problems of a launch form one sequence; CTA c
 // owns a contiguous run of it, balanced by packed bytes (two CTAs of 16 warps
